@@ -1,0 +1,286 @@
+/*
+ * pa_oracle.c -- plain, slow, fp64 CPU oracle for paged decode attention over an
+ * FP8 (e4m3) or BF16 paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call this
+ * file; only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It
+ * shares no code, header, table or constant with the CUDA library: it is written
+ * from the definitions below, in double precision, with no blocking or fusion.
+ *
+ * What it computes (one output row per query token, per query head):
+ *
+ *   Row map.  Request r owns query rows [cu_q[r], cu_q[r+1]); row tok of it is
+ *     cu_q[r] + tok.  Requests are recovered from cu_seqlens_q, never by dividing a
+ *     flat row index by a maximum query length (ROCm/ATOM PR 2122, "fix(minimax-m3):
+ *     unblock fp8 KV cache and EAGLE3 spec decode on the vLLM plugin", section 2,
+ *     "A decode segment must be uniform before a decode kernel may have it").
+ *
+ *   Causal cutoff.  Row tok of a request with context length L and q_len query
+ *     tokens attends positions p < L - q_len + tok + 1 (same page, section 2, the
+ *     index-topk cutoff "seq_len - max_query_len + tok + 1", read with the request's
+ *     own q_len).  context_lens[r] counts the request's own new tokens.
+ *
+ *   Key set.  Dense: every position p < min(L, cutoff).  Sparse: the positions of
+ *     the request's selected logical pages (entries < 0 are padding), restricted to
+ *     p < L and p < cutoff (ROCm/ATOM PR 2614, "Change": sparse decode reuses the
+ *     dense paged-decode contract).
+ *
+ *   Gather.  phys = block_table[r][p / page_size], slot o = p % page_size; the code
+ *     sits at k_cache[((phys * Hkv + h) * page_size + o) * D + d].
+ *
+ *   Explicit dequantisation (vLLM PR 52060, "[ROCm][Perf] Fold scalar KV scales in
+ *     MiniMax-M3 sparse attention", "Test Plan": outputs are compared against a
+ *     dequantised reference):
+ *       K^[p][d] = dec(code) * ks, ks = per-token k_scale[phys][h][o], or the scalar,
+ *       or 1 for a BF16 cache whose values are read exactly.  Same for V^.
+ *
+ *   Attention.  s_p = sm_scale * sum_d q[d] * K^[p][d] (q read exactly from bf16),
+ *     w_p = exp(s_p - max s) / sum exp(s - max s), out[d] = sum_p w_p V^[p][d],
+ *     lse = max s + log(sum exp(s - max s)).  An empty key set gives out = 0 and
+ *     lse = -inf.
+ *
+ * dec() is the OCP e4m3fn decoding (bias 7, subnormals 2^-6 * m/8, no infinities,
+ * S.1111.111 is NaN, largest finite 448); bf16 is decoded from its bit fields.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_KV_E4M3 0
+#define ORACLE_KV_BF16 1
+#define ORACLE_SCALE_NONE 0
+#define ORACLE_SCALE_SCALAR 1
+#define ORACLE_SCALE_PER_TOKEN 2
+
+typedef struct oracle_problem {
+  int32_t num_seqs, num_kv_heads, group_size, head_dim, page_size;
+  int32_t kv_dtype, scale_mode;
+  int64_t num_pages;
+  const uint16_t *q;            /* [rows, Hkv*group, D] bf16 bit patterns */
+  const void *k_cache;          /* [num_pages, Hkv, page_size, D] e4m3 codes or bf16 bits */
+  const void *v_cache;
+  const float *k_scale;         /* per-token: [num_pages, Hkv, page_size] */
+  const float *v_scale;
+  double k_scale_scalar, v_scale_scalar;
+  const int32_t *block_table;   /* [num_seqs, bt_stride] */
+  int32_t bt_stride;
+  const int32_t *context_lens;  /* [num_seqs] */
+  const int32_t *cu_seqlens_q;  /* [num_seqs + 1] */
+  const int32_t *selected;      /* [num_seqs, sel_stride] logical pages, -1 = padding; NULL = dense */
+  int32_t sel_stride;
+  const int32_t *num_selected;  /* [num_seqs] */
+  double sm_scale;
+} oracle_problem;
+
+/* OCP e4m3fn: s eeee mmm. */
+double oracle_dec_e4m3(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 3) & 0xF;
+  int m = code & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* bfloat16: s eeeeeeee mmmmmmm (bias 127). */
+double oracle_dec_bf16(uint16_t bits) {
+  int s = (bits >> 15) & 1;
+  int e = (bits >> 7) & 0xFF;
+  int m = bits & 0x7F;
+  double v;
+  if (e == 0xFF) return m ? NAN : (s ? -INFINITY : INFINITY);
+  if (e == 0)
+    v = ldexp((double)m / 128.0, -126);
+  else
+    v = ldexp(1.0 + (double)m / 128.0, e - 127);
+  return s ? -v : v;
+}
+
+/* The set of attended positions for (request r, query token tok): written into keys[],
+ * returns the count.  Order: ascending position for dense, selected-list order for
+ * sparse.  keys must hold max(context_len, num_selected * page_size) entries. */
+static int64_t key_set(const oracle_problem *pb, int r, int tok, int64_t *keys) {
+  int64_t L = pb->context_lens[r];
+  int64_t qlen = (int64_t)pb->cu_seqlens_q[r + 1] - pb->cu_seqlens_q[r];
+  int64_t cut = L - qlen + tok + 1;
+  int64_t lim = cut < L ? cut : L;
+  int64_t n = 0;
+  if (pb->selected == NULL) {
+    for (int64_t p = 0; p < lim; ++p) keys[n++] = p;
+  } else {
+    int64_t ns = pb->num_selected[r];
+    for (int64_t i = 0; i < ns; ++i) {
+      int64_t sp = pb->selected[(int64_t)r * pb->sel_stride + i];
+      if (sp < 0) continue;
+      for (int64_t o = 0; o < pb->page_size; ++o) {
+        int64_t p = sp * pb->page_size + o;
+        if (p < lim) keys[n++] = p;
+      }
+    }
+  }
+  return n;
+}
+
+/* e4m3 values of all 256 codes, each filled by oracle_dec_e4m3 itself. */
+static double e4m3_value[256];
+static pthread_once_t e4m3_once = PTHREAD_ONCE_INIT;
+static void fill_e4m3_values(void) {
+  for (int c = 0; c < 256; ++c) e4m3_value[c] = oracle_dec_e4m3((uint8_t)c);
+}
+
+static double dequant(const oracle_problem *pb, const void *cache, const float *scale_pt,
+                      double scale_scalar, int64_t phys, int h, int64_t o, int d) {
+  int64_t tok_index = (phys * pb->num_kv_heads + h) * pb->page_size + o;
+  int64_t idx = tok_index * pb->head_dim + d;
+  double x;
+  if (pb->kv_dtype == ORACLE_KV_E4M3)
+    x = e4m3_value[((const uint8_t *)cache)[idx]];
+  else
+    x = oracle_dec_bf16(((const uint16_t *)cache)[idx]);
+  if (pb->scale_mode == ORACLE_SCALE_PER_TOKEN) return x * (double)scale_pt[tok_index];
+  if (pb->scale_mode == ORACLE_SCALE_SCALAR) return x * scale_scalar;
+  return x;
+}
+
+/* One (request, kv head) pair: all of its rows and query heads. */
+static void decode_one(const oracle_problem *pb, int r, int h, double *out, double *lse,
+                       int64_t *keys, double *scores, double *qd) {
+  const int D = pb->head_dim, g = pb->group_size;
+  const int Hq = pb->num_kv_heads * g;
+  const int64_t row0 = pb->cu_seqlens_q[r];
+  const int qlen = pb->cu_seqlens_q[r + 1] - pb->cu_seqlens_q[r];
+  for (int tok = 0; tok < qlen; ++tok) {
+    const int64_t row = row0 + tok;
+    const int64_t n = key_set(pb, r, tok, keys);
+    for (int i = 0; i < g; ++i) {
+      const int head = h * g + i;
+      const uint16_t *qv = pb->q + (row * Hq + head) * D;
+      for (int d = 0; d < D; ++d) qd[d] = oracle_dec_bf16(qv[d]);
+      double *o = out + (row * Hq + head) * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      if (n == 0) {
+        if (lse) lse[row * Hq + head] = -INFINITY;
+        continue;
+      }
+      double smax = -INFINITY;
+      for (int64_t j = 0; j < n; ++j) {
+        const int64_t p = keys[j];
+        const int64_t phys = pb->block_table[(int64_t)r * pb->bt_stride + p / pb->page_size];
+        const int64_t slot = p % pb->page_size;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+          acc += qd[d] *
+                 dequant(pb, pb->k_cache, pb->k_scale, pb->k_scale_scalar, phys, h, slot, d);
+        scores[j] = pb->sm_scale * acc;
+        if (scores[j] > smax) smax = scores[j];
+      }
+      double z = 0.0;
+      for (int64_t j = 0; j < n; ++j) z += exp(scores[j] - smax);
+      for (int64_t j = 0; j < n; ++j) {
+        const int64_t p = keys[j];
+        const int64_t phys = pb->block_table[(int64_t)r * pb->bt_stride + p / pb->page_size];
+        const int64_t slot = p % pb->page_size;
+        const double w = exp(scores[j] - smax) / z;
+        for (int d = 0; d < D; ++d)
+          o[d] += w * dequant(pb, pb->v_cache, pb->v_scale, pb->v_scale_scalar, phys, h, slot, d);
+      }
+      if (lse) lse[row * Hq + head] = smax + log(z);
+    }
+  }
+}
+
+typedef struct {
+  const oracle_problem *pb;
+  double *out, *lse;
+  int64_t max_keys;
+  int next;
+  pthread_mutex_t mu;
+  int failed;
+} pool_t;
+
+static void *worker(void *arg) {
+  pool_t *P = (pool_t *)arg;
+  int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)(P->max_keys + 1));
+  double *scores = (double *)malloc(sizeof(double) * (size_t)(P->max_keys + 1));
+  double *qd = (double *)malloc(sizeof(double) * (size_t)P->pb->head_dim);
+  if (!keys || !scores || !qd) {
+    pthread_mutex_lock(&P->mu);
+    P->failed = 1;
+    pthread_mutex_unlock(&P->mu);
+    free(keys);
+    free(scores);
+    free(qd);
+    return NULL;
+  }
+  const int items = P->pb->num_seqs * P->pb->num_kv_heads;
+  for (;;) {
+    pthread_mutex_lock(&P->mu);
+    int it = P->next++;
+    pthread_mutex_unlock(&P->mu);
+    if (it >= items) break;
+    decode_one(P->pb, it / P->pb->num_kv_heads, it % P->pb->num_kv_heads, P->out, P->lse, keys,
+               scores, qd);
+  }
+  free(keys);
+  free(scores);
+  free(qd);
+  return NULL;
+}
+
+/* Runs the oracle with up to nthreads worker threads over (request, kv head) pairs.
+ * out: [rows, Hq, D] fp64; lse: [rows, Hq] fp64 natural-log LSE (may be NULL).
+ * Returns 0 on success, -1 on a bad argument or allocation failure. */
+int oracle_decode(const oracle_problem *pb, double *out, double *lse, int nthreads) {
+  if (!pb || !out || pb->num_seqs < 0 || pb->head_dim <= 0 || pb->group_size <= 0 ||
+      pb->num_kv_heads <= 0 || pb->page_size <= 0)
+    return -1;
+  pthread_once(&e4m3_once, fill_e4m3_values);
+  int64_t max_keys = 1;
+  for (int r = 0; r < pb->num_seqs; ++r) {
+    int64_t n = pb->context_lens[r];
+    if (pb->selected) {
+      int64_t m = (int64_t)pb->num_selected[r] * pb->page_size;
+      if (m > n) n = m;
+    }
+    if (n > max_keys) max_keys = n;
+  }
+  pool_t P;
+  P.pb = pb;
+  P.out = out;
+  P.lse = lse;
+  P.max_keys = max_keys;
+  P.next = 0;
+  P.failed = 0;
+  pthread_mutex_init(&P.mu, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 512) nthreads = 512;
+  pthread_t th[512];
+  int started = 0;
+  for (int i = 0; i < nthreads; ++i) {
+    if (pthread_create(&th[i], NULL, worker, &P) != 0) break;
+    ++started;
+  }
+  if (started == 0) worker(&P);
+  for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+  pthread_mutex_destroy(&P.mu);
+  return P.failed ? -1 : 0;
+}
+
+/* The attended positions of one (request, query token), in key-set order, for the
+ * gather and row-map checks.  Returns the count, or -1 if cap is too small. */
+int64_t oracle_key_positions(const oracle_problem *pb, int r, int tok, int64_t *keys,
+                             int64_t cap) {
+  int64_t need = pb->context_lens[r];
+  if (pb->selected) {
+    int64_t m = (int64_t)pb->num_selected[r] * pb->page_size;
+    if (m > need) need = m;
+  }
+  if (need > cap) return -1;
+  return key_set(pb, r, tok, keys);
+}

@@ -1,0 +1,272 @@
+"""Seeded synthetic inputs for paged decode attention over an FP8 (e4m3) KV cache.
+
+This module only makes data: it holds none of the attention arithmetic, so that the
+CUDA path and the fp64 CPU oracle can both consume the very same bytes.  Every array
+is a numpy array on the host; callers copy what they need to the device.
+
+Workload recipe (the shapes and value distributions of the MiniMax-M3 decode
+workloads on the source pages: one KV head per tensor-parallel rank, 16 query heads
+per KV head, head_dim 128, pages of 128 tokens, ROCm/ATOM PR 2122 section 2 and
+vLLM PR 52060 "Serve command"):
+
+* Q is bf16, drawn N(0, 1) in fp32 and rounded to bf16 (round to nearest even).
+* K and V are drawn N(0, 1) in fp32.  Per-token mode quantises every (page, KV head,
+  slot) row of head_dim values to e4m3 with scale = amax / 448 (fp32 scale, codes
+  from x / scale clamped to +-448 and rounded to nearest even by the torch cast);
+  an all-zero row gets scale 0 and codes 0.  Scalar mode draws one K and one V scale
+  uniform in [0.005, 0.05] and quantises x / scale the same way (saturation at +-448
+  is part of the data).  The BF16 control stores the dequantised values code * scale
+  rounded to bf16.
+* Block tables map every logical page of every request to a distinct physical page
+  of a shared pool, through a seeded random permutation of the pool.
+* Ragged speculative-decode batches carry cu_seqlens_q; uniform batches also carry
+  it (row r * q_len), so both sides see one row map.
+* Sparse batches carry a per-request list of logical page indices (sampled without
+  replacement, always holding the request's last page), padded with -1.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+E4M3_MAX = 448.0
+
+
+@dataclasses.dataclass
+class Problem:
+    num_seqs: int
+    num_kv_heads: int
+    group_size: int
+    head_dim: int
+    page_size: int
+    kv_dtype: str                      # "fp8" | "bf16"
+    scale_mode: str                    # "none" | "scalar" | "per_token"
+    q: np.ndarray                      # uint16 bf16 bits [rows, Hq, D]
+    k_cache: np.ndarray                # uint8 codes or uint16 bf16 bits [P, Hkv, ps, D]
+    v_cache: np.ndarray
+    k_scale: Optional[np.ndarray]      # float32 [P, Hkv, ps] (per-token mode)
+    v_scale: Optional[np.ndarray]
+    k_scale_scalar: float
+    v_scale_scalar: float
+    block_table: np.ndarray            # int32 [B, stride]
+    context_lens: np.ndarray           # int32 [B]
+    cu_seqlens_q: np.ndarray           # int32 [B + 1]
+    uniform_q_len: Optional[int]       # q_len when every request has the same count
+    selected: Optional[np.ndarray]     # int32 [B, sel_stride], -1 padded
+    num_selected: Optional[np.ndarray]  # int32 [B]
+    sm_scale: float
+    name: str = ""
+
+    @property
+    def num_rows(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def q_lens(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens_q).astype(np.int32)
+
+    @property
+    def max_q_len(self) -> int:
+        return int(self.q_lens.max()) if self.num_seqs else 0
+
+
+# ----------------------------------------------------------------------------- data
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 values -> bf16 bit patterns (torch cast, round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """fp32 values (already in code units) -> e4m3fn codes, clamped to +-448."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).clamp_(-E4M3_MAX, E4M3_MAX)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def e4m3_values(codes: np.ndarray) -> np.ndarray:
+    """e4m3fn codes -> fp32 values via the torch dtype (used only to build the BF16 control)."""
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float32).numpy()
+
+
+def quantize_per_token(x: np.ndarray):
+    """Per-row quantisation over the last axis: scale = amax / 448."""
+    amax = np.abs(x).max(axis=-1).astype(np.float32)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    codes = e4m3_codes(x / safe[..., None])
+    codes[scale == 0] = 0
+    return codes, scale
+
+
+def quantize_scalar(x: np.ndarray, scale: float):
+    return e4m3_codes(x / np.float32(scale))
+
+
+def _normal(rng: np.random.Generator, shape) -> np.ndarray:
+    return rng.standard_normal(size=shape, dtype=np.float32)
+
+
+def _fill_pages(rng, pages: np.ndarray, Hkv, ps, D, scale_mode, kv_dtype, k_out, v_out,
+                ks_out, vs_out, kss, vss, chunk=1024):
+    """Draw N(0,1) K/V for the listed physical pages and store their encoding."""
+    for i in range(0, len(pages), chunk):
+        idx = pages[i:i + chunk]
+        for which, out, sout, ss in ((0, k_out, ks_out, kss), (1, v_out, vs_out, vss)):
+            x = _normal(rng, (len(idx), Hkv, ps, D))
+            if scale_mode == "per_token":
+                codes, sc = quantize_per_token(x)
+            elif scale_mode == "scalar":
+                codes, sc = quantize_scalar(x, ss), None
+            else:
+                codes, sc = None, None
+            if kv_dtype == "fp8":
+                out[idx] = codes
+                if sc is not None:
+                    sout[idx] = sc
+            else:
+                if codes is None:
+                    out[idx] = bf16_bits(x)
+                else:
+                    val = e4m3_values(codes)
+                    val = val * (sc[..., None] if sc is not None else np.float32(ss))
+                    out[idx] = bf16_bits(val)
+
+
+def make_problem(seed: int, *, num_seqs: int, context_lens: Sequence[int],
+                 q_lens: Sequence[int], num_kv_heads: int = 1, group_size: int = 16,
+                 head_dim: int = 128, page_size: int = 128, kv_dtype: str = "fp8",
+                 scale_mode: str = "per_token", pool_pages: Optional[int] = None,
+                 selected_pages: Optional[int] = None, block_table_pad: int = 0,
+                 only_selected_data: bool = False, name: str = "") -> Problem:
+    """General seeded problem.  kv_dtype "bf16" with scale_mode "none" draws bf16 values
+    directly; "bf16" with another scale_mode stores the dequantised e4m3 values."""
+    rng = np.random.default_rng(seed)
+    B, Hkv, g, D, ps = num_seqs, num_kv_heads, group_size, head_dim, page_size
+    L = np.asarray(context_lens, dtype=np.int64)
+    ql = np.asarray(q_lens, dtype=np.int64)
+    assert L.shape == (B,) and ql.shape == (B,)
+    npg = (L + ps - 1) // ps
+    need = int(npg.sum())
+    P = max(need, 1) if pool_pages is None else int(pool_pages)
+    assert P >= need, "pool too small"
+    perm = rng.permutation(P).astype(np.int32)
+    stride = max(int(npg.max()) if B else 1, 1) + block_table_pad
+    bt = np.full((B, stride), -1, dtype=np.int32)
+    off = 0
+    for r in range(B):
+        bt[r, :npg[r]] = perm[off:off + npg[r]]
+        off += int(npg[r])
+
+    sel = nsel = None
+    if selected_pages is not None:
+        sel = np.full((B, selected_pages), -1, dtype=np.int32)
+        nsel = np.zeros(B, dtype=np.int32)
+        for r in range(B):
+            n = int(npg[r])
+            k = min(selected_pages, n)
+            if n == 0:
+                continue
+            others = rng.choice(n - 1, size=k - 1, replace=False) if k > 1 else np.zeros(0, int)
+            pick = np.concatenate([others, [n - 1]]).astype(np.int32)
+            rng.shuffle(pick)
+            sel[r, :k] = pick
+            nsel[r] = k
+
+    kss = float(rng.uniform(0.005, 0.05)) if scale_mode == "scalar" else 1.0
+    vss = float(rng.uniform(0.005, 0.05)) if scale_mode == "scalar" else 1.0
+    cdt = np.uint8 if kv_dtype == "fp8" else np.uint16
+    k_cache = np.zeros((P, Hkv, ps, D), dtype=cdt)
+    v_cache = np.zeros((P, Hkv, ps, D), dtype=cdt)
+    per_tok = scale_mode == "per_token" and kv_dtype == "fp8"
+    k_scale = np.zeros((P, Hkv, ps), dtype=np.float32) if per_tok else None
+    v_scale = np.zeros((P, Hkv, ps), dtype=np.float32) if per_tok else None
+    if only_selected_data and sel is not None:
+        used = np.unique(np.concatenate(
+            [bt[r, sel[r, :nsel[r]]] for r in range(B) if nsel[r] > 0] or [np.zeros(0, np.int32)]))
+    else:
+        used = np.arange(P, dtype=np.int64)
+    used = np.asarray(used, dtype=np.int64)
+    _fill_pages(rng, used, Hkv, ps, D, scale_mode, kv_dtype, k_cache, v_cache,
+                k_scale, v_scale, kss, vss)
+
+    rows = int(ql.sum())
+    q = bf16_bits(_normal(rng, (rows, Hkv * g, D)))
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(ql)
+    uni = int(ql[0]) if B and np.all(ql == ql[0]) else None
+    eff_mode = scale_mode if kv_dtype == "fp8" else "none"
+    return Problem(num_seqs=B, num_kv_heads=Hkv, group_size=g, head_dim=D, page_size=ps,
+                   kv_dtype=kv_dtype, scale_mode=eff_mode, q=q, k_cache=k_cache,
+                   v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
+                   k_scale_scalar=kss if eff_mode == "scalar" else 1.0,
+                   v_scale_scalar=vss if eff_mode == "scalar" else 1.0,
+                   block_table=bt, context_lens=L.astype(np.int32), cu_seqlens_q=cu,
+                   uniform_q_len=uni, selected=sel, num_selected=nsel,
+                   sm_scale=1.0 / float(np.sqrt(D)), name=name)
+
+
+# --------------------------------------------------------------------- named workloads
+
+def tiny_dense(seed: int = 0) -> Problem:
+    """4 requests, Hkv 1, group 16, D 128, page 16, context uniform in [1, 300], q_len 1,
+    block table a random permutation of a 128-page pool."""
+    rng = np.random.default_rng(seed + 1000)
+    L = rng.integers(1, 301, size=4)
+    return make_problem(seed, num_seqs=4, context_lens=L, q_lens=[1] * 4, page_size=16,
+                        pool_pages=128, name="tiny dense decode")
+
+
+def dense_8k(seed: int = 1, kv_dtype: str = "fp8", num_seqs: int = 32) -> Problem:
+    """Batch 32, every context 8192, page 128, q_len 1, per-token e4m3 K/V (or the BF16
+    control with the same dequantised values)."""
+    return make_problem(seed, num_seqs=num_seqs, context_lens=[8192] * num_seqs,
+                        q_lens=[1] * num_seqs, page_size=128, kv_dtype=kv_dtype,
+                        scale_mode="per_token", name="dense decode 8K")
+
+
+def long_128k(seed: int = 2, scale_mode: str = "scalar", num_seqs: int = 8,
+              context: int = 131072) -> Problem:
+    """Batch 8, every context 131072, page 128, q_len 1, scalar or per-token scales."""
+    return make_problem(seed, num_seqs=num_seqs, context_lens=[context] * num_seqs,
+                        q_lens=[1] * num_seqs, page_size=128, scale_mode=scale_mode,
+                        name="long-context decode 128K")
+
+
+def ragged_spec(seed: int = 3, batch: str = "A") -> Problem:
+    """(A) 31 requests, 30 with q_len 4 and one (seeded position) with q_len 1 (121 rows);
+    (B) 4 requests with q_len [4, 4, 6, 2] (16 rows).  Contexts uniform in [1024, 32768]."""
+    rng = np.random.default_rng(seed + 1000 + (0 if batch == "A" else 1))
+    if batch == "A":
+        ql = [4] * 31
+        ql[int(rng.integers(0, 31))] = 1
+    else:
+        ql = [4, 4, 6, 2]
+    L = rng.integers(1024, 32769, size=len(ql))
+    return make_problem(seed + (0 if batch == "A" else 100), num_seqs=len(ql), context_lens=L,
+                        q_lens=ql, page_size=128, name=f"ragged speculative decode {batch}")
+
+
+def sparse_selected(seed: int = 4, num_seqs: int = 32, context: int = 131072,
+                    selected: int = 64, only_selected_data: bool = True) -> Problem:
+    """Batch 32, context 131072 (1024 pages), 64 selected pages per request (always the
+    last page), q_len 1 for the first half of the requests and 4 for the second half."""
+    ql = [1] * (num_seqs // 2) + [4] * (num_seqs - num_seqs // 2)
+    return make_problem(seed, num_seqs=num_seqs, context_lens=[context] * num_seqs,
+                        q_lens=ql, page_size=128, selected_pages=selected,
+                        only_selected_data=only_selected_data, name="sparse selected-page decode")
+
+
+def kv_bytes_per_token(p: Problem) -> int:
+    """Algorithmic bytes of one attended (token, KV head): K and V rows plus scales."""
+    if p.kv_dtype == "bf16":
+        return 4 * p.head_dim
+    return 2 * p.head_dim + (8 if p.scale_mode == "per_token" else 0)

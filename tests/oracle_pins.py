@@ -1,0 +1,391 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each pin takes an OracleLib (the real build, or a mutated copy) and raises
+AssertionError when the oracle disagrees with
+  * a library routine (torch's float8_e4m3fn / bfloat16 decoding, torch's fp64
+    scaled_dot_product_attention and logsumexp over a gather built with torch
+    indexing),
+  * a closed form (equal keys give the mean of V, q = 0 gives the uniform mean and
+    log n, one key gives that key's V, two keys give a logistic weight),
+  * an invariant stated by the source pages (folded scales equal per-element
+    dequantisation, unit scales with bf16-exact values equal bf16 attention, a ragged
+    batch equals its uniform pieces row by row, a sparse run over every page equals
+    the dense run, scalar mode equals per-token mode with equal scales), or
+  * a worked example printed on the pages (the [4, 4, 6, 2] ragged batch, 121 rows).
+"""
+from __future__ import annotations
+
+import dataclasses
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from paged_fp8_kv_04_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TOL = 1e-11
+
+
+# ------------------------------------------------------------------ independent brute force
+
+def _dequant_cache(p, which):
+    cache = p.k_cache if which == "k" else p.v_cache
+    if p.kv_dtype == "fp8":
+        x = torch.from_numpy(np.ascontiguousarray(cache)).view(torch.float8_e4m3fn).to(torch.float64)
+    else:
+        x = torch.from_numpy(np.ascontiguousarray(cache).view(np.int16)).view(torch.bfloat16)
+        x = x.to(torch.float64)
+    if p.scale_mode == "per_token":
+        s = p.k_scale if which == "k" else p.v_scale
+        x = x * torch.from_numpy(s).to(torch.float64)[..., None]
+    elif p.scale_mode == "scalar":
+        x = x * float(p.k_scale_scalar if which == "k" else p.v_scale_scalar)
+    return x
+
+
+def _q64(p):
+    return torch.from_numpy(p.q.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+
+
+def _positions(p, r):
+    """Candidate positions of request r (before the causal cutoff), in gather order."""
+    L, ps = int(p.context_lens[r]), p.page_size
+    if p.selected is None:
+        return torch.arange(L, dtype=torch.int64)
+    pages = [int(x) for x in p.selected[r, :p.num_selected[r]] if x >= 0]
+    if not pages:
+        return torch.zeros(0, dtype=torch.int64)
+    pos = (torch.tensor(pages)[:, None] * ps + torch.arange(ps)[None, :]).reshape(-1)
+    return pos[pos < L]
+
+
+def brute_force(p):
+    """fp64 torch attention: gather with tensor indexing, SDPA with a boolean mask."""
+    K, V, Q = _dequant_cache(p, "k"), _dequant_cache(p, "v"), _q64(p)
+    g, D = p.group_size, p.head_dim
+    out = torch.zeros(Q.shape, dtype=torch.float64)
+    lse = torch.full(Q.shape[:2], float("-inf"), dtype=torch.float64)
+    bt = torch.from_numpy(p.block_table).to(torch.int64)
+    for r in range(p.num_seqs):
+        r0, r1 = int(p.cu_seqlens_q[r]), int(p.cu_seqlens_q[r + 1])
+        ql = r1 - r0
+        if ql == 0:
+            continue
+        pos = _positions(p, r)
+        phys = bt[r, pos // p.page_size]
+        slot = pos % p.page_size
+        tok = torch.arange(ql)[:, None]
+        mask = pos[None, :] < (int(p.context_lens[r]) - ql + tok + 1)       # [ql, n]
+        for h in range(p.num_kv_heads):
+            Kr, Vr = K[phys, h, slot], V[phys, h, slot]                    # [n, D]
+            Qr = Q[r0:r1, h * g:(h + 1) * g].transpose(0, 1)                # [g, ql, D]
+            if pos.numel() == 0:
+                continue
+            o = F.scaled_dot_product_attention(Qr, Kr[None].expand(g, -1, -1),
+                                               Vr[None].expand(g, -1, -1),
+                                               attn_mask=mask[None].expand(g, -1, -1),
+                                               scale=p.sm_scale)
+            s = (Qr @ Kr.T) * p.sm_scale
+            s = s.masked_fill(~mask[None], float("-inf"))
+            lz = torch.logsumexp(s, dim=-1)                                 # [g, ql]
+            empty = ~mask.any(dim=-1)                                       # [ql]
+            o = torch.where(empty[None, :, None], torch.zeros_like(o), o)
+            out[r0:r1, h * g:(h + 1) * g] = o.transpose(0, 1)
+            lse[r0:r1, h * g:(h + 1) * g] = lz.transpose(0, 1)
+    return out.numpy(), lse.numpy()
+
+
+def _close(a, b, tol=TOL, what=""):
+    a, b = np.asarray(a), np.asarray(b)
+    fin = np.isfinite(b)
+    assert np.array_equal(np.isfinite(a), fin), f"{what}: finiteness differs"
+    assert np.array_equal(a[~fin], b[~fin]), f"{what}: infinities differ"
+    err = np.max(np.abs(a[fin] - b[fin])) if fin.any() else 0.0
+    assert err <= tol, f"{what}: max abs diff {err}"
+
+
+# ----------------------------------------------------------------------------- problems
+
+def _small(seed, **kw):
+    base = dict(num_seqs=3, context_lens=[37, 5, 20], q_lens=[1, 1, 1], page_size=16,
+                head_dim=32, group_size=4)
+    base.update(kw)
+    return synth.make_problem(seed, **base)
+
+
+def _mutate(p, **kw):
+    return dataclasses.replace(p, **kw)
+
+
+# --------------------------------------------------------------------------------- pins
+
+def pin_e4m3_all_codes(lib):
+    """Every one of the 256 e4m3fn codes decodes as torch.float8_e4m3fn does."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([lib.dec_e4m3(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "NaN codes differ"
+    m = ~np.isnan(ref)
+    assert np.array_equal(got[m], ref[m]), "e4m3 values differ"
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def pin_bf16_all_patterns(lib):
+    """Every bf16 bit pattern decodes as torch.bfloat16 does (NaNs as NaN)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([lib.dec_bf16(int(b)) for b in bits[::7]])
+    r = ref[::7]
+    assert np.array_equal(np.isnan(got), np.isnan(r))
+    m = ~np.isnan(r)
+    assert np.array_equal(got[m], r[m]), "bf16 values differ"
+
+
+def pin_brute_dense_per_token(lib):
+    p = _small(11)
+    _close(lib.decode(p)[0], brute_force(p)[0], what="out")
+    _close(lib.decode(p)[1], brute_force(p)[1], what="lse")
+
+
+def pin_brute_dense_scalar(lib):
+    p = _small(12, scale_mode="scalar")
+    o, l = lib.decode(p)
+    bo, bl = brute_force(p)
+    _close(o, bo, what="out")
+    _close(l, bl, what="lse")
+
+
+def pin_brute_bf16_kv(lib):
+    p = _small(13, kv_dtype="bf16", scale_mode="none")
+    o, l = lib.decode(p)
+    bo, bl = brute_force(p)
+    _close(o, bo, what="out")
+    _close(l, bl, what="lse")
+
+
+def pin_brute_two_kv_heads(lib):
+    """Hkv = 2 so that the head -> KV-head map and the cache's head stride both matter."""
+    p = _small(14, num_kv_heads=2, context_lens=[40, 17, 3])
+    o, l = lib.decode(p)
+    bo, bl = brute_force(p)
+    _close(o, bo, what="out")
+    _close(l, bl, what="lse")
+
+
+def pin_brute_ragged_causal(lib):
+    """Ragged q_len [4, 4, 6, 2] with the cutoff L - q_len + tok + 1 (and one L < q_len)."""
+    p = _small(15, num_seqs=5, context_lens=[50, 9, 33, 18, 3], q_lens=[4, 4, 6, 2, 5])
+    o, l = lib.decode(p)
+    bo, bl = brute_force(p)
+    _close(o, bo, what="out")
+    _close(l, bl, what="lse")
+
+
+def pin_brute_sparse(lib):
+    p = _small(16, num_seqs=3, context_lens=[100, 60, 77], q_lens=[1, 3, 2], selected_pages=3)
+    sel = p.selected.copy()
+    sel[1, 2] = -1                                   # padding inside the count
+    p = _mutate(p, selected=sel)
+    o, l = lib.decode(p)
+    bo, bl = brute_force(p)
+    _close(o, bo, what="out")
+    _close(l, bl, what="lse")
+
+
+def pin_closed_form_equal_keys(lib):
+    """All keys equal: uniform weights, out = mean of V^ over the causal key set."""
+    p = _small(17, num_seqs=2, context_lens=[30, 19], q_lens=[3, 1])
+    k = p.k_cache.copy()
+    k[:] = k[0, 0, 0]
+    ks = np.full_like(p.k_scale, 0.01)
+    p = _mutate(p, k_cache=k, k_scale=ks)
+    o, l = lib.decode(p)
+    V = _dequant_cache(p, "v").numpy()
+    for r in range(p.num_seqs):
+        ql = p.q_lens[r]
+        for tok in range(ql):
+            n = int(p.context_lens[r]) - ql + tok + 1
+            pos = np.arange(n)
+            vh = V[p.block_table[r, pos // p.page_size], 0, pos % p.page_size]
+            row = p.cu_seqlens_q[r] + tok
+            for i in range(p.group_size):
+                assert np.max(np.abs(o[row, i] - vh.mean(axis=0))) < TOL
+
+
+def pin_closed_form_zero_query(lib):
+    """q = 0: every score is 0, out = mean of V^, lse = log(n)."""
+    p = _small(18, context_lens=[23, 1, 64], q_lens=[2, 1, 1])
+    p = _mutate(p, q=np.zeros_like(p.q))
+    o, l = lib.decode(p)
+    V = _dequant_cache(p, "v").numpy()
+    for r in range(p.num_seqs):
+        ql = p.q_lens[r]
+        for tok in range(ql):
+            n = int(p.context_lens[r]) - ql + tok + 1
+            pos = np.arange(n)
+            vh = V[p.block_table[r, pos // p.page_size], 0, pos % p.page_size].mean(axis=0)
+            row = p.cu_seqlens_q[r] + tok
+            assert np.max(np.abs(o[row] - vh[None])) < TOL
+            assert np.max(np.abs(l[row] - np.log(n))) < TOL
+
+
+def pin_closed_form_one_and_two_keys(lib):
+    """One key: out = V^[0], lse = its score.  Two keys: logistic weights."""
+    p = _small(19, num_seqs=2, context_lens=[1, 2], q_lens=[1, 1])
+    o, l = lib.decode(p)
+    K, V, Q = (_dequant_cache(p, "k").numpy(), _dequant_cache(p, "v").numpy(),
+               _q64(p).numpy())
+    b0 = p.block_table[0, 0]
+    s = Q[0] @ K[b0, 0, 0] * p.sm_scale
+    assert np.max(np.abs(o[0] - V[b0, 0, 0][None])) < TOL
+    assert np.max(np.abs(l[0] - s)) < TOL
+    b1 = p.block_table[1, 0]
+    s0 = Q[1] @ K[b1, 0, 0] * p.sm_scale
+    s1 = Q[1] @ K[b1, 0, 1] * p.sm_scale
+    w1 = 1.0 / (1.0 + np.exp(s0 - s1))
+    want = (1 - w1)[:, None] * V[b1, 0, 0][None] + w1[:, None] * V[b1, 0, 1][None]
+    assert np.max(np.abs(o[1] - want)) < TOL
+    assert np.max(np.abs(l[1] - np.logaddexp(s0, s1))) < TOL
+
+
+def pin_invariant_folded_scales(lib):
+    """Per-token K scale folded into the score column and V scale into P (vLLM PR 52060,
+    "Suggested Fix") equals explicit per-element dequantisation."""
+    p = _small(20, context_lens=[45, 12, 31], q_lens=[1, 2, 1])
+    o, _ = lib.decode(p)
+    codes_k = torch.from_numpy(p.k_cache).view(torch.float8_e4m3fn).to(torch.float64)
+    codes_v = torch.from_numpy(p.v_cache).view(torch.float8_e4m3fn).to(torch.float64)
+    ks = torch.from_numpy(p.k_scale).to(torch.float64)
+    vs = torch.from_numpy(p.v_scale).to(torch.float64)
+    Q = _q64(p)
+    for r in range(p.num_seqs):
+        ql = p.q_lens[r]
+        L = int(p.context_lens[r])
+        pos = torch.arange(L)
+        phys = torch.from_numpy(p.block_table[r]).long()[pos // p.page_size]
+        sl = pos % p.page_size
+        for tok in range(ql):
+            n = L - ql + tok + 1
+            row = p.cu_seqlens_q[r] + tok
+            raw = Q[row] @ codes_k[phys[:n], 0, sl[:n]].T                  # [g, n]
+            s = raw * (ks[phys[:n], 0, sl[:n]] * p.sm_scale)[None]
+            w = torch.softmax(s, dim=-1) * vs[phys[:n], 0, sl[:n]][None]
+            want = w @ codes_v[phys[:n], 0, sl[:n]]
+            assert np.max(np.abs(o[row] - want.numpy())) < TOL
+
+
+def pin_invariant_unit_scales_bf16(lib):
+    """Unit per-token scales with bf16-exact values equal the BF16-KV run exactly."""
+    p = _small(21, context_lens=[29, 16, 8], q_lens=[1, 1, 2])
+    p8 = _mutate(p, k_scale=np.ones_like(p.k_scale), v_scale=np.ones_like(p.v_scale))
+    kb = synth.bf16_bits(synth.e4m3_values(p.k_cache))
+    vb = synth.bf16_bits(synth.e4m3_values(p.v_cache))
+    pb = _mutate(p8, kv_dtype="bf16", scale_mode="none", k_cache=kb, v_cache=vb,
+                 k_scale=None, v_scale=None)
+    o8, l8 = lib.decode(p8)
+    ob, lb = lib.decode(pb)
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
+
+
+def pin_invariant_ragged_equals_uniform(lib):
+    """A ragged batch equals, row by row, the uniform batches of its pieces."""
+    p = _small(22, num_seqs=4, context_lens=[40, 33, 51, 20], q_lens=[4, 4, 6, 2])
+    o, l = lib.decode(p)
+    for r in range(p.num_seqs):
+        one = _mutate(p, num_seqs=1, block_table=p.block_table[r:r + 1],
+                      context_lens=p.context_lens[r:r + 1],
+                      cu_seqlens_q=np.array([0, p.q_lens[r]], dtype=np.int32),
+                      q=p.q[p.cu_seqlens_q[r]:p.cu_seqlens_q[r + 1]], uniform_q_len=p.q_lens[r])
+        o1, l1 = lib.decode(one)
+        a, b = p.cu_seqlens_q[r], p.cu_seqlens_q[r + 1]
+        assert np.array_equal(o[a:b], o1) and np.array_equal(l[a:b], l1)
+
+
+def pin_invariant_sparse_all_pages_is_dense(lib):
+    p = _small(23, context_lens=[70, 16, 33], q_lens=[1, 2, 1])
+    npg = (p.context_lens + p.page_size - 1) // p.page_size
+    sel = np.full((p.num_seqs, int(npg.max())), -1, dtype=np.int32)
+    rng = np.random.default_rng(5)
+    for r in range(p.num_seqs):
+        sel[r, :npg[r]] = rng.permutation(npg[r])
+    ps = _mutate(p, selected=sel, num_selected=npg.astype(np.int32))
+    _close(lib.decode(ps)[0], lib.decode(p)[0], tol=1e-13, what="out")
+    _close(lib.decode(ps)[1], lib.decode(p)[1], tol=1e-13, what="lse")
+
+
+def pin_invariant_scalar_is_uniform_per_token(lib):
+    p = _small(24, scale_mode="scalar")
+    ks = np.full((p.num_pages, 1, p.page_size), np.float32(p.k_scale_scalar), dtype=np.float32)
+    vs = np.full((p.num_pages, 1, p.page_size), np.float32(p.v_scale_scalar), dtype=np.float32)
+    p2 = _mutate(p, scale_mode="per_token", k_scale=ks, v_scale=vs,
+                 k_scale_scalar=float(np.float32(p.k_scale_scalar)),
+                 v_scale_scalar=float(np.float32(p.v_scale_scalar)))
+    p1 = _mutate(p, k_scale_scalar=float(np.float32(p.k_scale_scalar)),
+                 v_scale_scalar=float(np.float32(p.v_scale_scalar)))
+    assert np.array_equal(lib.decode(p1)[0], lib.decode(p2)[0])
+
+
+def _golden_rowmap():
+    path = os.path.join(GOLDEN, "rowmap_4_4_6_2.txt")
+    rows = []
+    meta = {}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if "=" in line:
+                k, v = line.split("=", 1)
+                meta[k.strip()] = [int(x) for x in v.split(",")]
+                continue
+            rows.append([int(x) for x in line.split()])
+    return meta, np.array(rows)
+
+
+def pin_golden_ragged_4_4_6_2(lib):
+    """The page's ragged batch [4, 4, 6, 2]: 16 rows, divisible by 4 yet ragged.  The
+    oracle's key sets follow the fixture's (request, tok, cutoff) per row."""
+    meta, rows = _golden_rowmap()
+    ql, L = meta["q_lens"], meta["context_lens"]
+    p = _small(25, num_seqs=4, context_lens=L, q_lens=ql)
+    assert p.num_rows == 16 and p.num_rows % 4 == 0
+    for row, r, tok, cut in rows:
+        assert p.cu_seqlens_q[r] + tok == row
+        keys = lib.key_positions(p, r, tok)
+        assert np.array_equal(keys, np.arange(cut)), (row, r, tok, cut)
+    # the division map the page warns about disagrees on some rows of this batch
+    div = [(row // 4, row % 4) for row in range(16)]
+    assert any((r, t) != d for (_, r, t, _), d in zip(rows, div))
+
+
+def pin_golden_121_rows(lib):
+    """30 requests with q_len 4 plus one with q_len 1 give 121 rows (121 = 30*4 + 1);
+    each row's key set ends at its own cutoff."""
+    ql = [4] * 30 + [1]
+    ql[7], ql[30] = 1, 4
+    L = [20 + 3 * i for i in range(31)]
+    p = synth.make_problem(26, num_seqs=31, context_lens=L, q_lens=ql, page_size=16,
+                           head_dim=16, group_size=2)
+    assert p.num_rows == 121
+    for r in (6, 7, 8, 30):
+        for tok in range(ql[r]):
+            keys = lib.key_positions(p, r, tok)
+            assert keys.size == L[r] - ql[r] + tok + 1 and keys[-1] == keys.size - 1
+
+
+def pin_golden_q_shape_225280(lib):
+    """110 rows of [Hkv=1, g=16, D=128] is the 225280-element query of the page, which
+    a [27, 4, 1, 16, 128] reshape (108 rows) cannot hold."""
+    assert 110 * 1 * 16 * 128 == 225280 and 27 * 4 * 16 * 128 != 225280
+    ql = [4] * 26 + [6]
+    assert sum(ql) == 110
+    p = synth.make_problem(27, num_seqs=27, context_lens=[8] * 27, q_lens=ql, page_size=16,
+                           head_dim=128, group_size=16)
+    assert p.q.size == 225280
+    o, _ = lib.decode(p)
+    assert o.shape == (110, 16, 128)
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

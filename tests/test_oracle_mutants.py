@@ -1,0 +1,52 @@
+"""The pins are strong enough: each plausible mistake planted in a copy of the oracle
+source (a dropped term, a wrong sign, bias or index, swapped operands) makes at least
+one pin fail.  The mistakes are planted only in throw-away copies, on the CPU."""
+import os
+
+import pytest
+
+import oracle_pins
+from oracle import oracle as O
+
+MUTANTS = {
+    "cutoff_off_by_one": ("int64_t cut = L - qlen + tok + 1;", "int64_t cut = L - qlen + tok;"),
+    "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_exp": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "bf16_bias": ("ldexp(1.0 + (double)m / 128.0, e - 127)",
+                  "ldexp(1.0 + (double)m / 128.0, e - 126)"),
+    "block_table_first_page_only": ("p / pb->page_size]", "0]"),
+    "slot_shift": ("const int64_t slot = p % pb->page_size;",
+                   "const int64_t slot = (p + 1) % pb->page_size;"),
+    "per_token_scale_first_slot": ("scale_pt[tok_index]",
+                                   "scale_pt[(phys * pb->num_kv_heads + h) * pb->page_size]"),
+    "scalar_v_scale_dropped": ("return x * scale_scalar;", "return x;"),
+    "sm_scale_dropped": ("scores[j] = pb->sm_scale * acc;", "scores[j] = acc;"),
+    "v_reads_k": ("pb->v_cache, pb->v_scale, pb->v_scale_scalar",
+                  "pb->k_cache, pb->k_scale, pb->k_scale_scalar"),
+    "sparse_ignores_cutoff": ("if (p < lim) keys[n++] = p;", "if (p < L) keys[n++] = p;"),
+    "sparse_padding_as_page0": ("if (sp < 0) continue;", "if (sp < 0) sp = 0;"),
+    "head_map_transposed": ("const int head = h * g + i;",
+                            "const int head = i * pb->num_kv_heads + h;"),
+    "kv_head_stride_dropped": ("(phys * pb->num_kv_heads + h) * pb->page_size + o",
+                               "(phys * pb->num_kv_heads) * pb->page_size + o"),
+    "row_tok_reversed": ("const int64_t row = row0 + tok;",
+                         "const int64_t row = row0 + (qlen - 1 - tok);"),
+    "lse_without_max": ("smax + log(z)", "log(z)"),
+    "softmax_sign": ("exp(scores[j] - smax)", "exp(smax - scores[j])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = O.source_text()
+    assert old in src, f"mutation anchor for {name} not found"
+    lib = O.OracleLib(O.build_variant(src.replace(old, new), str(tmp_path / f"m_{name}.so")))
+    failed = []
+    for pin in oracle_pins.PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+            break
+    assert failed, f"no pin caught mutant {name}"
