@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark of paged FP8-KV decode attention on GB300: one JSON line on rank 0.
+
+Metric: achieved HBM GB/s (algorithmic bytes / time; % of the measured peak) and query
+rows/s.  Default workload: dense decode at 8K -- batch 32, one KV head, 16 query heads
+per KV head, head_dim 128, pages of 128 tokens, every context 8192, q_len 1, per-token
+e4m3 K/V scales.  A step is one pa_decode call over the whole batch.  The timed region
+replays a CUDA graph of K back-to-back calls that cycle through several copies of the
+KV cache whose total exceeds 3x the L2, so that every call reads its KV from HBM.
+
+--impl reference times the fp64 CPU oracle (the reference implementation of this
+build) on the host cores, on bounded samples of the same workload.
+Multi-GPU: the path is replicated (independent batches per GPU, no collective); value
+is the sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "FP8-KV paged decode: achieved HBM GB/s (% of GB300 peak), query rows/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dense8k",
+                    choices=["dense8k", "bf16ctl", "long128k_scalar", "long128k", "ragged",
+                             "sparse"])
+    ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = balanced)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def make_workload(name):
+    from paged_fp8_kv_04_gb300 import synth
+    if name == "dense8k":
+        p = synth.dense_8k(1)
+        desc = ("dense decode 8K: batch 32, Hkv 1, group 16, head_dim 128, page 128, "
+                "context 8192, q_len 1, per-token e4m3 K/V")
+    elif name == "bf16ctl":
+        p = synth.dense_8k(1, kv_dtype="bf16")
+        desc = "dense decode 8K BF16-KV control (same shapes, dequantised values in bf16)"
+    elif name == "long128k_scalar":
+        p = synth.long_128k(2, scale_mode="scalar")
+        desc = "long-context decode 128K: batch 8, context 131072, q_len 1, scalar e4m3 scales"
+    elif name == "long128k":
+        p = synth.long_128k(2, scale_mode="per_token")
+        desc = "long-context decode 128K: batch 8, context 131072, q_len 1, per-token e4m3 scales"
+    elif name == "ragged":
+        p = synth.ragged_spec(3, "A")
+        desc = "ragged speculative decode: 31 requests (30 x q_len 4 + 1 x q_len 1, 121 rows)"
+    else:
+        p = synth.sparse_selected(4)
+        desc = ("sparse selected-page decode: batch 32, context 131072, 64 selected pages, "
+                "q_len 1/4 (80 rows)")
+    return p, desc
+
+
+def algorithmic_bytes(p):
+    """KV bytes of every attended (token, KV head) + Q + out + page indices."""
+    from paged_fp8_kv_04_gb300 import synth
+    per_tok = synth.kv_bytes_per_token(p)
+    ps = p.page_size
+    tokens = 0
+    pages = 0
+    for r in range(p.num_seqs):
+        L = int(p.context_lens[r])
+        if p.selected is None:
+            tokens += L
+            pages += (L + ps - 1) // ps
+        else:
+            sel = [int(x) for x in p.selected[r, :p.num_selected[r]] if x >= 0]
+            tokens += sum(min(ps, L - s * ps) for s in sel if s * ps < L)
+            pages += len(sel) * 2  # selected entry + block-table entry
+    kv = tokens * p.num_kv_heads * per_tok
+    qo = 2 * p.num_rows * p.num_kv_heads * p.group_size * p.head_dim * 2
+    return kv + qo + 4 * pages * p.num_kv_heads, kv
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def time_oracle(p, sample_rows_target_s=0.5):
+    """The oracle on a bounded sample of p on all host cores: (GB/s, rows/s, sample text)."""
+    from oracle import oracle as O
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    O.decode(p, threads=cores)
+    dt = time.perf_counter() - t0
+    total, kv = algorithmic_bytes(p)
+    return total / dt / 1e9, p.num_rows / dt, dt, cores
+
+
+def bench_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    import dataclasses
+    p, desc = make_workload(args.workload)
+    cores = os.cpu_count() or 1
+    # Each step: `cores` requests of the workload, each truncated to n leading tokens, so
+    # that the whole --steps/--warmup run stays within about two minutes.
+    idx = list(range(min(cores, p.num_seqs)))
+    from oracle import oracle as O
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_util import subset
+
+    def sample(n):
+        q = subset(p, idx)
+        L = np.minimum(q.context_lens, n).astype(np.int32)
+        if q.selected is not None:
+            return dataclasses.replace(q, context_lens=np.maximum(L, q.q_lens))
+        return dataclasses.replace(q, context_lens=np.maximum(L, q.q_lens))
+
+    probe = sample(256)
+    t0 = time.perf_counter()
+    O.decode(probe, threads=cores)
+    per_tok = (time.perf_counter() - t0) / 256
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    n = int(max(16, min(int(p.context_lens.max()), budget / max(per_tok, 1e-9))))
+    q = sample(n)
+    for _ in range(args.warmup):
+        O.decode(q, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.decode(q, threads=cores)
+    dt = time.perf_counter() - t0
+    total, _ = algorithmic_bytes(q)
+    value = total * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "sample": f"{len(idx)} requests x first {n} tokens per step"},
+        "rows_per_s": q.num_rows * args.steps / dt,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{len(idx)} requests of the workload, each cut to its first {n} tokens"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_ours(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        __graft_entry__.build()
+    from paged_fp8_kv_04_gb300 import device as dv
+
+    p, desc = make_workload(args.workload)
+    d = dv.to_device(p, dev)
+    plan = dv.plan_for(p, device=dev, partition_tokens=args.partition)
+    total_bytes, kv_bytes = algorithmic_bytes(p)
+
+    # Rotating copies of the KV cache (and scales) so that no call finds its KV in L2.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool_bytes = sum(d[k].numel() * d[k].element_size() for k in
+                     ("k_cache", "v_cache", "k_scale", "v_scale") if d.get(k) is not None)
+    touched = max(kv_bytes, 1)
+    npools = max(3, int(math.ceil(3 * l2 / touched)) + 1)
+    npools = min(npools, max(3, int(40e9 // max(pool_bytes, 1))))
+    pools = [d] + [dict(d, **{k: d[k].clone() for k in ("k_cache", "v_cache", "k_scale", "v_scale")
+                              if d.get(k) is not None}) for _ in range(npools - 1)]
+    out = torch.empty(d["q"].shape, dtype=torch.bfloat16, device=dev)
+    keep = []
+    args_list = []
+    for pd in pools:
+        kw = dv.call_kwargs(p, pd)
+        args_list.append(plan.args(pd["q"], pd["k_cache"], pd["v_cache"], pd["block_table"],
+                                   pd["context_lens"], out=out, keep=keep, **kw))
+    stream = torch.cuda.Stream(device=dev)
+
+    # warm-up: W direct calls
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            plan.decode_args(args_list[i % npools], stream=stream)
+    torch.cuda.synchronize(dev)
+    assert plan.device_status() == 0
+
+    # one CUDA graph of `chunk` calls; the timed region replays it K / chunk times
+    K = args.steps
+    chunk = max(c for c in range(1, min(K, 1000) + 1) if K % c == 0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            plan.decode_args(args_list[i % npools], stream=stream)
+    g.replay()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K // chunk):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    flags = plan.device_status()
+
+    # per-launch time of direct (non-graph) calls, for reference
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    nd = min(K, 2000)
+    with torch.cuda.stream(stream):
+        e2.record(stream)
+        for i in range(nd):
+            plan.decode_args(args_list[i % npools], stream=stream)
+        e3.record(stream)
+    torch.cuda.synchronize(dev)
+    direct_us = e2.elapsed_time(e3) / nd * 1e3
+
+    t_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    sec = t_max / 1e3
+    value = world * total_bytes * K / sec / 1e9
+    rows_s = world * p.num_rows * K / sec
+    us_per_call = ms / K * 1e3
+
+    # end to end through the C ABI: pinned host inputs -> device, decode, output -> host
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in d.items()}
+        dbuf = {k: torch.empty_like(v) for k, v in d.items()}
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        kw = dv.call_kwargs(p, dbuf)
+        a_e2e = plan.args(dbuf["q"], dbuf["k_cache"], dbuf["v_cache"], dbuf["block_table"],
+                          dbuf["context_lens"], out=out, keep=keep, **kw)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out.numel() * out.element_size()
+        steps_e2e = 30
+        with torch.cuda.stream(stream):
+            for it in range(steps_e2e + 3):
+                if it == 3:
+                    torch.cuda.synchronize(dev)
+                    t0 = time.perf_counter()
+                for k in host:
+                    dbuf[k].copy_(host[k], non_blocking=True)
+                plan.decode_args(a_e2e, stream=stream)
+                hout.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        dt = (time.perf_counter() - t0) / steps_e2e
+        e2e = {"value": world * total_bytes / dt / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": dt * 1e3}
+
+    if rank != 0:
+        return
+    peak, peak_kind = peak_hbm()
+    achieved = total_bytes / (us_per_call * 1e-6) / 1e9
+    cpu = None
+    if not args.no_cpu:
+        gbs, rps, dt, cores = time_oracle(p)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"the full batch once ({p.num_rows} rows), {dt:.1f} s wall",
+               "rows_per_s": rps}
+    info = plan.info()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 KV, f16 mma, f32 accumulate"
+        if p.kv_dtype == "fp8" else "bf16 mma, f32 accumulate", "data": "synthetic",
+        "config": {"workload": desc, "l2": f"{npools} rotating KV copies ({npools * pool_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
+                   "timed": "CUDA graph replay of back-to-back pa_decode calls",
+                   "grid_ctas": info["grid_ctas"], "stages": info["stages"],
+                   "partition_tokens": args.partition},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "rows_per_s": rows_s,
+        "us_per_call_graph": us_per_call, "us_per_call_direct": direct_us,
+        "algorithmic_bytes_per_call": int(total_bytes),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clk,
+        "device_flags": flags,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

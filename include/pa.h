@@ -1,0 +1,208 @@
+/*
+ * pa.h -- C ABI of libpagedfp8: paged decode attention over an FP8 (e4m3) KV cache
+ * with per-token or scalar K/V scales (and a BF16-KV control), for grouped-query
+ * attention with ragged speculative-decode query lengths, split-K over long contexts
+ * with a log-sum-exp merge, and a sparse selected-page variant.  sm_103a (GB300).
+ *
+ * Sources of the operation (the pages are pull-request threads):
+ *  - ROCm/ATOM PR 2614, "Change": dense max-q-len-1 per-token FP8 decode and sparse
+ *    decode share one paged-decode contract; "Validation": the per-token kernel
+ *    needs split-K.
+ *  - ROCm/ATOM PR 2710, review "Must fix" 1 and "Should fix" 2: scratch is sized
+ *    from a bounded set of capacity buckets and reused; an unsupported call is
+ *    refused at set-up, not raised mid-run; "Smaller": partition scratch
+ *    (exp_sums, max_logits, temporary_output).
+ *  - ROCm/ATOM PR 2122 ("fix(minimax-m3): unblock fp8 KV cache and EAGLE3 spec decode
+ *    on the vLLM plugin"), section 1: FP8 caches are raw bytes; section 2: a decode
+ *    segment must be measured as uniform, rows map to requests through
+ *    cu_seqlens_q, and row tok attends positions < seq_len - q_len + tok + 1.
+ *  - vLLM PR 52060 ("[ROCm][Perf] Fold scalar KV scales in MiniMax-M3 sparse
+ *    attention"), "Suggested Fix": a scalar K scale folds into the score scale and a
+ *    scalar V scale is applied once to the normalised fp32 accumulator; per-token
+ *    scales stay per token.
+ *
+ * Conventions for every call:
+ *  - Device pointers are caller-owned device memory; the library allocates no device
+ *    memory at any time.  Its only scratch is the caller's workspace, sized once per
+ *    plan by pa_plan_workspace_size.
+ *  - Errors are returned as pa_status_t; no call aborts, throws or prints.
+ *  - pa_decode performs no host synchronisation and no allocation, and returns as
+ *    soon as its kernel is enqueued on the given stream.
+ */
+#ifndef PAGEDFP8_PA_H
+#define PAGEDFP8_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* a null pointer, a negative size or a value out of range */
+  PA_ERR_UNSUPPORTED = 2,   /* a shape or mode this library does not implement */
+  PA_ERR_CAPACITY = 3,      /* a call larger than its plan's capacity bucket */
+  PA_ERR_RAGGED = 4,        /* a uniform plan given ragged (or miscounted) query rows */
+  PA_ERR_ALIGN = 5,         /* a pointer without the required 16-byte alignment */
+  PA_ERR_CUDA = 6,          /* a CUDA runtime or driver call failed */
+  PA_ERR_DEVICE_DATA = 7,   /* the kernel flagged bad data (see PA_DEV_* flags) */
+  PA_ERR_WORKSPACE = 8      /* the workspace is null, misaligned or too small */
+} pa_status_t;
+
+enum { PA_KV_FP8_E4M3 = 0, PA_KV_BF16 = 1 };
+enum { PA_SCALE_NONE = 0, PA_SCALE_SCALAR = 1, PA_SCALE_PER_TOKEN = 2 };
+enum { PA_Q_UNIFORM = 0, PA_Q_RAGGED = 1 };
+enum { PA_OUT_BF16 = 0, PA_OUT_F32 = 1 };
+
+/* Device status flags, OR-ed into the plan's workspace by the kernels.  A flagged
+ * work item is skipped (its pages are not read); nothing traps.  Read them with
+ * pa_plan_get_device_status. */
+#define PA_DEV_BAD_PAGE      0x01u  /* a block-table entry outside [0, num_pages) */
+#define PA_DEV_BAD_CONTEXT   0x02u  /* context_len < 0, > max_context_len, or more pages than the block-table stride */
+#define PA_DEV_BAD_QLEN      0x04u  /* a request's q_len < 0 or > the plan's q_len, or context_len < q_len */
+#define PA_DEV_NOT_UNIFORM   0x08u  /* uniform plan, but cu_seqlens_q[r] != r * q_len */
+#define PA_DEV_BAD_SELECTED  0x10u  /* num_selected outside [0, selected_stride], or a selected page outside [-1, pages of the request) */
+#define PA_DEV_Q_RANGE       0x20u  /* a query value outside the f16 range (|q| > 65504) */
+#define PA_DEV_TIMEOUT       0x40u  /* a bounded wait inside a kernel gave up (the output is incomplete) */
+#define PA_DEV_DUMP_RANGE    0x80u  /* pa_debug_gather's buffer was too small for the schedule */
+
+/* Plan descriptor: the capacity bucket and the fixed shape of every call on the plan
+ * (ROCm/ATOM PR 2710 review, "Must fix" 1: size the plan by a capacity bucket).
+ * Supported: head_dim 128, group_size 16, page_size in {16, 32, 64, 128},
+ * kv_dtype FP8 with scale_mode SCALAR or PER_TOKEN, or BF16 with scale_mode NONE;
+ * q_len 1..8; max_batch 1..4096. */
+typedef struct pa_plan_desc {
+  int32_t num_kv_heads;       /* Hkv >= 1; query heads = Hkv * group_size, head j uses KV head j / group_size */
+  int32_t group_size;         /* query heads sharing one KV head */
+  int32_t head_dim;           /* D */
+  int32_t page_size;          /* tokens per page */
+  int32_t kv_dtype;           /* PA_KV_* */
+  int32_t scale_mode;         /* PA_SCALE_* */
+  int32_t q_mode;             /* PA_Q_UNIFORM: every request has q_len rows; PA_Q_RAGGED: rows from cu_seqlens_q */
+  int32_t q_len;              /* uniform: rows per request; ragged: the most rows one request may have */
+  int32_t max_batch;          /* most requests per call */
+  int32_t max_rows;           /* most query rows per call */
+  int32_t max_context_len;    /* longest context (tokens, counting the request's own q_len new tokens) */
+  int32_t max_selected_pages; /* 0: dense-only plan; else the most selected pages per request in sparse calls */
+  int32_t partition_tokens;   /* 0: balanced persistent schedule (one CTA per SM, equal tile counts);
+                                 else fixed split-K partitions of this many tokens (multiple of 128) */
+  int32_t out_dtype;          /* PA_OUT_BF16 (round to nearest even) or PA_OUT_F32 */
+  int32_t num_sms;            /* 0: the current device's SM count; > 0: use this count (sizing without a GPU) */
+  int32_t reserved[3];        /* must be 0 */
+} pa_plan_desc_t;
+
+/* One decode call.  Layouts are dense row-major; rows = query tokens. */
+typedef struct pa_decode_args {
+  const void *q;                   /* device bf16 [num_rows, Hkv*group, head_dim], 16-B aligned */
+  const void *k_cache;             /* device [num_pages, Hkv, page_size, head_dim]: e4m3 bytes (raw uint8 or
+                                      float8_e4m3fn storage, ROCm/ATOM PR 2122 section 1) or bf16; 16-B aligned */
+  const void *v_cache;             /* same layout as k_cache */
+  const float *k_scale;            /* device fp32 [num_pages, Hkv, page_size]; PER_TOKEN only, 16-B aligned */
+  const float *v_scale;            /* same; PER_TOKEN only */
+  float k_scale_scalar;            /* SCALAR only: one K scale for the whole cache */
+  float v_scale_scalar;            /* SCALAR only: one V scale */
+  int64_t num_pages;               /* physical pages in each cache (bounds every block-table entry) */
+  const int32_t *block_table;      /* device int32 [num_seqs, block_table_stride]: logical page -> physical page */
+  int32_t block_table_stride;      /* entries per block-table row */
+  int32_t num_seqs;                /* requests in this call (<= max_batch) */
+  const int32_t *context_lens;     /* device int32 [num_seqs]: tokens in each request's cache, own q_len included */
+  const int32_t *cu_seqlens_q;     /* device int32 [num_seqs + 1]: request r owns rows [cu[r], cu[r+1]);
+                                      required by RAGGED plans, optional for UNIFORM (then checked on device) */
+  const int32_t *cu_seqlens_q_host;/* host int32 [num_seqs + 1], optional: validated before launch */
+  const int32_t *selected_pages;   /* device int32 [num_seqs, selected_stride] logical page indices, -1 = padding;
+                                      NULL for a dense call */
+  const int32_t *num_selected;     /* device int32 [num_seqs]: entries used per row of selected_pages */
+  int32_t selected_stride;         /* entries per selected_pages row (<= max_selected_pages) */
+  int32_t num_rows;                /* query rows in this call (<= max_rows) */
+  float sm_scale;                  /* softmax scale, > 0 (1/sqrt(head_dim) for the workloads) */
+  int32_t reserved0;               /* must be 0 */
+  void *out;                       /* device [num_rows, Hkv*group, head_dim], bf16 or fp32 per the plan; 16-B aligned */
+  float *lse;                      /* device fp32 [num_rows, Hkv*group], optional: natural-log sum of exp of the
+                                      scores (-inf for an empty key set) */
+} pa_decode_args_t;
+
+/* Facts about a created plan (for tests and benchmarks). */
+typedef struct pa_plan_info {
+  int32_t grid_ctas;          /* CTAs per decode launch (balanced: the SM count) */
+  int32_t stages;             /* KV tiles in flight per CTA */
+  int32_t threads_per_cta;
+  int32_t tile_tokens;        /* tokens per KV tile (128) */
+  int64_t smem_bytes;         /* dynamic shared memory per CTA */
+  int64_t workspace_bytes;
+  int64_t partial_slots;      /* split-K partial (m, l, o) slots in the workspace */
+} pa_plan_info_t;
+
+typedef struct pa_plan pa_plan_t;
+
+/* Validates a descriptor without touching a GPU.  PA_ERR_UNSUPPORTED for an
+ * unimplemented shape or mode, PA_ERR_INVALID_ARG for an out-of-range field. */
+pa_status_t pa_plan_validate(const pa_plan_desc_t *desc);
+
+/* Workspace bytes a plan with this descriptor needs (a multiple of 256), or 0 if the
+ * descriptor is refused.  Queries the current device when desc->num_sms == 0. */
+size_t pa_plan_workspace_size(const pa_plan_desc_t *desc);
+
+/* Creates a plan bound to a caller-owned device workspace of at least
+ * pa_plan_workspace_size bytes (256-B aligned).  The workspace holds the split-K
+ * partials, per-request merge counters and the device status word; this call
+ * zero-fills its control part with a synchronous cudaMemset on the current device.
+ * The plan is immutable and reusable by any call within its bucket; calls that share
+ * a plan (and so its workspace) must be serialised on one stream.  On error *plan is
+ * set to NULL.  With d_workspace == NULL and workspace_bytes == 0 the plan is
+ * check-only: it makes no CUDA call, serves pa_decode_check (for refusing a serving
+ * configuration at start-up), and pa_decode on it returns PA_ERR_WORKSPACE. */
+pa_status_t pa_plan_create(const pa_plan_desc_t *desc, void *d_workspace, size_t workspace_bytes,
+                           pa_plan_t **plan);
+
+/* Host-only check of a call against its plan (capacity, mode, pointers, alignment,
+ * the host mirror of cu_seqlens_q).  Launches nothing.  pa_decode runs it first. */
+pa_status_t pa_decode_check(const pa_plan_t *plan, const pa_decode_args_t *args);
+
+/* Enqueues one decode on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * Refusals (PA_ERR_CAPACITY, PA_ERR_RAGGED, ...) happen before anything is enqueued.
+ * Rows of requests with an empty key set are written as zeros (lse -inf).  Data errors
+ * found on the device set PA_DEV_* flags instead of faulting. */
+pa_status_t pa_decode(pa_plan_t *plan, const pa_decode_args_t *args, void *stream);
+
+/* Synchronises the device, copies the plan's PA_DEV_* flags to *flags and, if clear
+ * is non-zero, resets them.  For tests and diagnostics, never on the hot path. */
+pa_status_t pa_plan_get_device_status(pa_plan_t *plan, uint32_t *flags, int clear);
+
+pa_status_t pa_plan_get_info(const pa_plan_t *plan, pa_plan_info_t *info);
+
+/* Frees the host-side plan (the workspace stays the caller's).  NULL is a no-op. */
+void pa_plan_destroy(pa_plan_t *plan);
+
+/* A static string naming the status. */
+const char *pa_status_string(pa_status_t status);
+
+/* ---- test hooks: exact integer / byte outputs of the row map and the page gather ---- */
+
+/* For every query row: (request, query token, causal cutoff) as int32 triples into the
+ * device buffer row_map [num_rows, 3], computed by the same device code that maps rows
+ * in pa_decode (ROCm/ATOM PR 2122, section 2).  Rows no request owns are left as is. */
+pa_status_t pa_debug_row_map(pa_plan_t *plan, const pa_decode_args_t *args, int32_t *row_map,
+                             void *stream);
+
+/* Bytes per KV tile in pa_debug_gather's output. */
+size_t pa_debug_gather_tile_bytes(const pa_plan_t *plan);
+
+/* Runs pa_decode's schedule and page-gather path (block table, selected pages, tile
+ * loads into shared memory) and, instead of attending, writes every tile it loaded to
+ * `dump` at its global tile index: a 128-byte header of int32 (request, KV head, tile,
+ * flags, context_len, q_len, first row, valid pages, then 8 first-positions and 8
+ * physical pages, -1 where a page slot is empty), the K tile and the V tile as
+ * [128 tokens][head_dim] elements with the swizzle undone, then (FP8 per-token) the
+ * 128 K and 128 V scales.  Tiles are numbered request-major, then KV head, then tile;
+ * dump must hold (number of tiles) * pa_debug_gather_tile_bytes bytes, given as
+ * dump_bytes (tiles past it set PA_DEV_DUMP_RANGE and are skipped). */
+pa_status_t pa_debug_gather(pa_plan_t *plan, const pa_decode_args_t *args, void *dump,
+                            size_t dump_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDFP8_PA_H */

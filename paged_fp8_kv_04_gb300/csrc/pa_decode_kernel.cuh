@@ -1,0 +1,202 @@
+// pa_decode_kernel.cuh -- kernel entry points: decode, gather dump, row map.
+#pragma once
+
+#include "pa_consumer.cuh"
+#include "pa_producer.cuh"
+
+namespace pa {
+
+// Copies one loaded stage to the gather dump (swizzle undone).  Header: 32 int32.
+template <int KVT, int SM>
+__device__ void dump_stage(const KParams &p, const Smem &sm, int s, int ctid, int tile_bytes) {
+  const StageMeta *mt = sm.meta(s);
+  const int gt = mt->gtile;
+  if ((int64_t)gt >= p.dump_tiles) {
+    if (ctid == 0) atomicOr(p.status, PA_DEV_DUMP_RANGE);
+    return;
+  }
+  uint8_t *dst = p.dump + (int64_t)gt * tile_bytes;
+  const int32_t *src_meta = reinterpret_cast<const int32_t *>(mt);
+  if (ctid < 32) {
+    int32_t v = 0;
+    if (ctid < 24) v = src_meta[ctid];
+    reinterpret_cast<int32_t *>(dst)[ctid] = v;
+  }
+  const uint32_t st = sm.stage(s);
+  const int row_bytes = (KVT == PA_KV_FP8_E4M3) ? kD : 2 * kD;
+  const int chunks = row_bytes / 16;  // 16-B chunks per token row
+  uint8_t *kv = dst + kDumpHeader;
+  for (int u = ctid; u < 2 * kTile * chunks; u += kNCW * 32) {
+    const int which = u / (kTile * chunks);  // 0 = K, 1 = V
+    const int rem = u - which * kTile * chunks;
+    const int row = rem / chunks, cc = rem - row * chunks;
+    uint32_t src;
+    if (KVT == PA_KV_FP8_E4M3)
+      src = st + which * 16384 + row * 128 + ((cc ^ (row & 7)) << 4);
+    else
+      src = st + which * 32768 + (cc >> 3) * 16384 + row * 128 + (((cc & 7) ^ (row & 7)) << 4);
+    const uint4 v = lds128(src);
+    *reinterpret_cast<uint4 *>(kv + which * kTile * row_bytes + row * row_bytes + cc * 16) = v;
+  }
+  if (KVT == PA_KV_FP8_E4M3 && SM == PA_SCALE_PER_TOKEN) {
+    uint8_t *sc = kv + 2 * kTile * row_bytes;
+    for (int u = ctid; u < 64; u += kNCW * 32)
+      *reinterpret_cast<uint4 *>(sc + 16 * u) = lds128(st + 32768 + 16 * u);
+  }
+}
+
+template <int KVT, int SM, bool DUMP>
+__device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int warp, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int ctid = warp * 32 + lane;
+  const int32_t *tstart = sm.tstart();
+  uint32_t cphase = 0;
+
+  // Requests without tiles (empty key set for every row): zero rows, lse = -inf.
+  if (!DUMP) {
+    const int Hq = p.Hkv * kG;
+    for (int r = blockIdx.x; r < p.num_seqs; r += gridDim.x) {
+      if (tstart[r + 1] != tstart[r]) continue;
+      uint32_t fl = 0;
+      const ReqInfo ri = request_info(p, r, fl);
+      if (ri.qlen <= 0) continue;
+      const int64_t e0 = (int64_t)ri.row0 * Hq * kD, n = (int64_t)ri.qlen * Hq * kD;
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int64_t e = 4 * ctid; e < n; e += 4 * kNCW * 32) store_out(p, e0 + e, z, 4);
+      if (p.lse != nullptr)
+        for (int e = ctid; e < ri.qlen * Hq; e += kNCW * 32)
+          p.lse[(int64_t)ri.row0 * Hq + e] = -INFINITY;
+    }
+  }
+  if (a >= b) return;
+
+  Frag f;
+  reset_state(f);
+  int mt = 1, ts = kNCW, mtile = 0, slice = 0, cut = 0;
+  bool active = false;
+  const int tile_bytes = (KVT == PA_KV_FP8_E4M3) ? (kDumpHeader + 2 * kTile * kD + 1024)
+                                                  : (kDumpHeader + 4 * kTile * kD);
+  const int n = b - a;
+  for (int i = 0; i < n; ++i) {
+    const int s = i % p.nstage;
+    if (!mbar_wait_bounded(sm.full(s), (i / p.nstage) & 1)) {
+      if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
+      break;
+    }
+    const StageMeta *meta = sm.meta(s);
+    const int flags = meta->flags, r = meta->r, h = meta->h;
+    const int qlen = meta->qlen, row0 = meta->row0, L = meta->L;
+    if (flags & F_BEGIN) {
+      mt = qlen;
+      ts = kNCW / mt;
+      active = warp < mt * ts;
+      mtile = warp % mt;
+      slice = warp / mt;
+      cut = L - qlen + mtile + 1;
+      if (!DUMP && active) {
+        load_q<KVT>(p, sm.qslot(meta->qslot) + mtile * kQRowBytes, g, t, f);
+        reset_state(f);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.qempty(meta->qslot));
+    }
+    if (DUMP) {
+      dump_stage<KVT, SM>(p, sm, s, ctid, tile_bytes);
+    } else if (active) {
+      const bool masked = (flags & F_MASK) != 0;
+      const int tps = kTile / ts;
+      const uint32_t st = sm.stage(s);
+      for (int tb = slice * tps; tb < (slice + 1) * tps; tb += 16) {
+        int pos0 = 0;
+        if (masked) {
+          const int pp = meta->page_pos[tb >> p.ps_shift];
+          pos0 = pp < 0 ? -1 : pp + (tb & (p.ps - 1)) + 2 * t;
+        }
+        if (KVT == PA_KV_FP8_E4M3)
+          chunk_fp8<SM>(p, st, tb, masked, pos0, cut, g, t, f);
+        else
+          chunk_bf16(p, st, tb, masked, pos0, cut, g, t, lane, f);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.empty(s));
+
+    if (DUMP || !(flags & F_END)) continue;
+
+    // ---- end of this CTA's part of sequence (r, h): merge the token slices -----------
+    for (int step = ts >> 1; step >= 1; step >>= 1) {
+      if (active && slice >= step && slice < 2 * step) put_state(sm, (slice - step) * mt + mtile, f, lane);
+      cons_sync(p, sm, cphase);
+      if (active && slice < step) merge_state(sm, slice * mt + mtile, f, lane);
+      cons_sync(p, sm, cphase);
+    }
+    const bool writer = active && slice == 0;
+    if (flags & F_WHOLE) {
+      if (writer) write_final<KVT>(p, f, row0 + mtile, h * kG, g, t);
+      continue;
+    }
+    const int nt = tstart[r + 1] - tstart[r];
+    const int gs = tstart[r] * p.Hkv + h * nt;
+    int c_first, nc;
+    seq_ctas(p, tstart, r, h, gs, gs + nt, c_first, nc);
+    if (writer) write_partial<KVT>(p, f, slot_of(blockIdx.x, c_first), mtile, g, t);
+    __threadfence();
+    cons_sync(p, sm, cphase);
+    if (ctid == 0) {
+      const int old = atomicAdd(p.counters + (r * p.Hkv + h), 1);
+      sm.misc()[M_LAST] = (old == nc - 1) ? 1 : 0;
+    }
+    cons_sync(p, sm, cphase);
+    if (sm.misc()[M_LAST]) {
+      __threadfence();
+      merge_partials(p, r, h, row0, qlen, c_first, nc, ctid);
+      if (ctid == 0) p.counters[r * p.Hkv + h] = 0;
+    }
+  }
+}
+
+template <int KVT, int SM, bool DUMP>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t mis = smem_u32(smem_raw) & 1023u;
+  Smem sm{smem_raw + ((1024u - mis) & 1023u), &p};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.nstage; ++s) {
+      mbar_init(sm.full(s), 1);
+      mbar_init(sm.empty(s), kNCW);
+    }
+    mbar_init(sm.qempty(0), kNCW);
+    mbar_init(sm.qempty(1), kNCW);
+    mbar_init(sm.consbar(), kNCW);
+    sm.misc()[M_ABORT] = 0;
+    sm.misc()[M_LAST] = 0;
+    fence_barrier_init();
+  }
+  scan_tiles(p, sm.tstart(), sm.misc() + M_WSUM, blockIdx.x == 0);
+  int a, b;
+  cta_range(p, sm.tstart(), blockIdx.x, a, b);
+  if (warp == kNCW) {
+    if (a < b) run_producer<KVT, SM>(p, sm, a, b);
+    return;
+  }
+  run_consumer<KVT, SM, DUMP>(p, sm, a, b, warp, lane);
+}
+
+// (request, query token, cutoff) of every row, through request_info -- the same map
+// the decode kernel uses.
+__global__ void row_map_kernel(const __grid_constant__ KParams p, int32_t *row_map) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= p.num_seqs) return;
+  uint32_t fl = 0;
+  const ReqInfo ri = request_info(p, r, fl);
+  for (int tok = 0; tok < ri.qlen; ++tok) {
+    const int row = ri.row0 + tok;
+    row_map[3 * row] = r;
+    row_map[3 * row + 1] = tok;
+    row_map[3 * row + 2] = ri.L - ri.qlen + tok + 1;
+  }
+  if (fl) atomicOr(p.status, fl);
+}
+
+}  // namespace pa

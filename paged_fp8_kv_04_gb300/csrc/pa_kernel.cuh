@@ -1,0 +1,253 @@
+// pa_kernel.cuh -- the paged decode attention kernel for sm_103a.
+//
+// One persistent CTA per SM (balanced schedule) or one CTA per fixed split-K partition.
+// Work is a list of KV tiles of 128 tokens: request-major, then KV head, then tile.
+// Dense tiles cover positions [128 t, 128 t + 128); sparse tiles cover 128 / page_size
+// consecutive entries of the request's selected-page list (ROCm/ATOM PR 2614,
+// "Change": sparse decode reuses the dense paged-decode contract).
+//
+// Warp roles in a CTA of 9 warps:
+//   warp 8     producer: walks the CTA's tile range, reads block-table (and selected-
+//              page) entries, and moves each page's K and V rows into a shared-memory
+//              stage with TMA (128-byte swizzle) plus the per-token scales and, at the
+//              start of a request, the request's query rows, all completing on the
+//              stage's mbarrier.
+//   warps 0-7  consumers: exact e4m3 -> f16 widening in registers, QK^T and PV on
+//              mma.sync tensor-core fragments, online softmax with warp shuffles,
+//              per-token K scale folded into the score column and V scale into P
+//              (vLLM PR 52060, "Suggested Fix"), a log-sum-exp merge across warps,
+//              and, when a request spans several CTAs, split-K partials merged by the
+//              last CTA to finish (ROCm/ATOM PR 2710 review, "Smaller": exp_sums,
+//              max_logits, temporary_output).
+// Every wait is bounded; a wait that gives up sets PA_DEV_TIMEOUT and the CTA drains.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "pa.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kD = 128;          // head_dim
+constexpr int kG = 16;           // query heads per KV head (rows of one m-tile)
+constexpr int kTile = 128;       // tokens per KV tile
+constexpr int kNCW = 8;          // consumer warps
+constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kMaxQ = 8;         // most query tokens per request (m-tiles)
+constexpr int kQRowBytes = kG * kD * 2;   // one query token's 16 heads, bf16
+constexpr int kMergeBytes = 4 * 8192 + 4 * 512;
+constexpr int kDumpHeader = 128;
+constexpr float kLn2 = 0.693147180559945309f;
+
+enum : int { F_BEGIN = 1, F_END = 2, F_MASK = 4, F_WHOLE = 8 };
+
+// Written by the producer before it arrives on the stage's full barrier.
+struct StageMeta {
+  int32_t r, h, tile, flags;
+  int32_t L, qlen, row0, nvalid;
+  int32_t page_pos[8];   // first position of each page slot of the tile, -1 = empty
+  int32_t page_phys[8];  // its physical page, -1 = empty
+  int32_t gtile, qslot, pad[6];
+};
+static_assert(sizeof(StageMeta) == 128, "meta size");
+
+struct KParams {
+  CUtensorMap tm_k;               // 2-D map over [num_pages * Hkv * page_size rows, row bytes]
+  CUtensorMap tm_v;
+  const uint16_t *q;
+  const float *k_scale, *v_scale;
+  const int32_t *block_table, *context_lens, *cu_q, *sel, *nsel;
+  void *out;
+  float *lse;
+  uint32_t *status;
+  int32_t *counters;              // [num_seqs * Hkv] arrivals of split-K partials
+  float *part_ml;                 // [slots][2][mmax]  (m in log2 units, l)
+  float *part_o;                  // [slots][mmax][128] (unnormalised)
+  uint8_t *dump;
+  int64_t dump_tiles;
+  int64_t num_pages;
+  float kfold;                    // score = acc * kfold (* k_scale[token] in per-token mode)
+  float pfold;                    // P' = p * v_scale[token] * pfold (per-token mode)
+  float vpost;                    // out = (o / l) * vpost
+  int32_t num_seqs, Hkv, ps, ps_shift, ppt, bt_stride, sel_stride, q_uniform, max_q, max_ctx;
+  int32_t num_rows, out_f32, sched_partition, part_tiles, maxch, grid, nstage, mmax, sparse;
+  int32_t off_q, qslot_bytes, off_merge, off_tstart, off_meta, off_bar, off_misc, stage_bytes;
+};
+
+// ------------------------------------------------------------------ per-request geometry
+
+struct ReqInfo {
+  int32_t L, qlen, row0, tiles;
+};
+
+// Rows, context and tile count of request r, from cu_seqlens_q (never a division of a
+// flat row index: ROCm/ATOM PR 2122, section 2) and context_lens.  Bad data gives 0
+// tiles and a PA_DEV_* flag.
+__device__ __forceinline__ ReqInfo request_info(const KParams &p, int r, uint32_t &fl) {
+  ReqInfo ri;
+  ri.L = p.context_lens[r];
+  if (p.q_uniform > 0) {
+    ri.qlen = p.q_uniform;
+    ri.row0 = r * p.q_uniform;
+    if (p.cu_q != nullptr && (p.cu_q[r] != ri.row0 || p.cu_q[r + 1] != ri.row0 + ri.qlen))
+      fl |= PA_DEV_NOT_UNIFORM;
+  } else {
+    ri.row0 = p.cu_q[r];
+    ri.qlen = p.cu_q[r + 1] - ri.row0;
+  }
+  ri.tiles = 0;
+  if (ri.qlen < 0 || ri.qlen > p.max_q || ri.row0 < 0 || ri.row0 + ri.qlen > p.num_rows) {
+    fl |= PA_DEV_BAD_QLEN;
+    ri.qlen = 0;
+    return ri;
+  }
+  if (ri.L < 0 || ri.L > p.max_ctx || ((ri.L + p.ps - 1) >> p.ps_shift) > p.bt_stride) {
+    fl |= PA_DEV_BAD_CONTEXT;
+    return ri;
+  }
+  if (ri.qlen == 0) return ri;
+  if (ri.L < ri.qlen) fl |= PA_DEV_BAD_QLEN;
+  if (p.sparse) {
+    int ns = p.nsel[r];
+    if (ns < 0 || ns > p.sel_stride) {
+      fl |= PA_DEV_BAD_SELECTED;
+      ns = ns < 0 ? 0 : p.sel_stride;
+    }
+    ri.tiles = (ns + p.ppt - 1) / p.ppt;
+  } else {
+    ri.tiles = (ri.L + kTile - 1) / kTile;
+  }
+  return ri;
+}
+
+// Exclusive prefix of tile counts over requests into tstart[0..B] (shared memory).
+__device__ void scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum, bool report) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = p.num_seqs;
+  const int per = (B + kThreads - 1) / kThreads;
+  const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+  uint32_t fl = 0;
+  int local = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int n = request_info(p, r, fl).tiles;
+    tstart[r] = n;
+    local += n;
+  }
+  int inc = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const int v = wsum[w];
+      wsum[w] = run;
+      run += v;
+    }
+    tstart[B] = run;
+  }
+  __syncthreads();
+  int run = wsum[warp] + inc - local;
+  for (int r = r0; r < r1; ++r) {
+    const int n = tstart[r];
+    tstart[r] = run;
+    run += n;
+  }
+  if (report && fl) atomicOr(p.status, fl);
+  __syncthreads();
+}
+
+// Global tile index -> (request, KV head, tile within the request's head).
+__device__ __forceinline__ void locate(const int32_t *tstart, int B, int Hkv, int gt, int &r,
+                                       int &h, int &tile) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {  // first r with tstart[r + 1] * Hkv > gt
+    const int mid = (lo + hi) >> 1;
+    if (tstart[mid + 1] * Hkv > gt)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  r = lo;
+  const int nt = tstart[r + 1] - tstart[r];
+  const int off = gt - tstart[r] * Hkv;
+  h = off / nt;
+  tile = off - h * nt;
+}
+
+// The CTA's tile range [a, b).
+__device__ __forceinline__ void cta_range(const KParams &p, const int32_t *tstart, int c, int &a,
+                                          int &b) {
+  const int T = tstart[p.num_seqs] * p.Hkv;
+  if (!p.sched_partition) {
+    const int C = (T + p.grid - 1) / p.grid;
+    a = min(T, c * C);
+    b = min(T, a + C);
+    return;
+  }
+  const int s = c / p.maxch, k = c - s * p.maxch;
+  const int r = s / p.Hkv, h = s - r * p.Hkv;
+  a = b = 0;
+  if (r >= p.num_seqs) return;
+  const int nt = tstart[r + 1] - tstart[r];
+  const int gs = tstart[r] * p.Hkv + h * nt, ge = gs + nt;
+  a = min(ge, gs + k * p.part_tiles);
+  b = min(ge, a + p.part_tiles);
+}
+
+// CTAs that hold partials of sequence (r, h) whose tiles are [gs, ge).
+__device__ __forceinline__ void seq_ctas(const KParams &p, const int32_t *tstart, int r, int h,
+                                         int gs, int ge, int &c_first, int &n) {
+  if (!p.sched_partition) {
+    const int T = tstart[p.num_seqs] * p.Hkv;
+    const int C = (T + p.grid - 1) / p.grid;
+    c_first = gs / C;
+    n = (ge - 1) / C - c_first + 1;
+  } else {
+    c_first = (r * p.Hkv + h) * p.maxch;
+    n = (ge - gs + p.part_tiles - 1) / p.part_tiles;
+  }
+}
+
+// Partial slot of CTA c for a sequence: the CTA where the sequence starts writes its
+// "tail" slot 2c + 1; every later CTA writes its "head" slot 2c.
+__device__ __forceinline__ int slot_of(int c, int c_first) { return c == c_first ? 2 * c + 1 : 2 * c; }
+
+// --------------------------------------------------------------------- shared-memory map
+
+struct Smem {
+  uint8_t *base;
+  const KParams *p;
+  __device__ uint32_t stage(int s) const { return smem_u32(base) + s * p->stage_bytes; }
+  __device__ uint32_t qslot(int k) const { return smem_u32(base) + p->off_q + k * p->qslot_bytes; }
+  __device__ uint32_t merge() const { return smem_u32(base) + p->off_merge; }
+  __device__ int32_t *tstart() const { return reinterpret_cast<int32_t *>(base + p->off_tstart); }
+  __device__ StageMeta *meta(int s) const {
+    return reinterpret_cast<StageMeta *>(base + p->off_meta) + s;
+  }
+  __device__ uint32_t full(int s) const { return smem_u32(base) + p->off_bar + 8 * s; }
+  __device__ uint32_t empty(int s) const {
+    return smem_u32(base) + p->off_bar + 8 * (p->nstage + s);
+  }
+  __device__ uint32_t qempty(int k) const {
+    return smem_u32(base) + p->off_bar + 8 * (2 * p->nstage + k);
+  }
+  __device__ uint32_t consbar() const { return smem_u32(base) + p->off_bar + 8 * (2 * p->nstage + 2); }
+  __device__ int32_t *misc() const { return reinterpret_cast<int32_t *>(base + p->off_misc); }
+};
+
+// misc[] words
+enum : int { M_ABORT = 0, M_LAST = 1, M_WSUM = 4 };  // M_WSUM.. holds 9 warp sums
+
+__device__ __forceinline__ void raise_flag(const KParams &p, const Smem &sm, uint32_t f) {
+  atomicOr(p.status, f);
+  if (f & PA_DEV_TIMEOUT) atomicExch(&sm.misc()[M_ABORT], 1);
+}
+
+}  // namespace pa

@@ -1,0 +1,235 @@
+"""Host-side checks of the C ABI: the library builds and exports every symbol pa.h
+declares, and plans and calls are refused at set-up exactly as documented.  Nothing
+here launches a kernel: calls are checked with pa_decode_check on check-only plans,
+whose fake device pointers are never dereferenced."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from paged_fp8_kv_04_gb300 import binding as B
+from paged_fp8_kv_04_gb300 import build as libbuild
+
+OK, INVALID, UNSUP, CAP, RAGGED, ALIGN, CUDA, DEVDATA, WS = range(9)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return B.lib()
+
+
+def test_exports_every_header_symbol(lib):
+    names = B.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in B.STATUS.items():
+        assert lib.pa_status_string(code).decode() == name
+
+
+def desc(**kw):
+    base = dict(max_batch=32, max_context_len=8192, num_sms=152)
+    base.update(kw)
+    return B.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(), OK),
+    (dict(group_size=8), UNSUP),
+    (dict(head_dim=64), UNSUP),
+    (dict(page_size=256), UNSUP),
+    (dict(page_size=16), OK),
+    (dict(scale_mode="none"), UNSUP),
+    (dict(kv_dtype="bf16"), UNSUP),
+    (dict(kv_dtype="bf16", scale_mode="none"), OK),
+    (dict(scale_mode="scalar"), OK),
+    (dict(q_len=0), INVALID),
+    (dict(q_len=9), UNSUP),
+    (dict(q_len=8, q_mode="ragged"), OK),
+    (dict(max_batch=4097), UNSUP),
+    (dict(max_batch=0), INVALID),
+    (dict(partition_tokens=100), UNSUP),
+    (dict(partition_tokens=512), OK),
+    (dict(out_dtype="f32"), OK),
+    (dict(num_kv_heads=0), UNSUP),
+])
+def test_plan_validation(lib, kw, want):
+    d = desc(**kw)
+    assert lib.pa_plan_validate(ctypes.byref(d)) == want
+    size = lib.pa_plan_workspace_size(ctypes.byref(d))
+    assert (size > 0) == (want == OK)
+
+
+def test_reserved_fields_must_be_zero(lib):
+    d = desc()
+    d.reserved[1] = 3
+    assert lib.pa_plan_validate(ctypes.byref(d)) == INVALID
+
+
+def test_workspace_size_is_bounded_and_deterministic(lib):
+    d = desc()
+    a = lib.pa_plan_workspace_size(ctypes.byref(d))
+    assert a == lib.pa_plan_workspace_size(ctypes.byref(desc())) and a % 256 == 0
+    # balanced schedule: partial slots scale with the SM count, not with the batch
+    big = lib.pa_plan_workspace_size(ctypes.byref(desc(max_batch=4096)))
+    assert big - a == (4096 - 32) * 4 // 256 * 256 or big > a
+    assert lib.pa_plan_workspace_size(ctypes.byref(desc(q_len=4, q_mode="ragged"))) > a
+    # fixed partitions: one slot pair per (request, head, partition)
+    part = lib.pa_plan_workspace_size(ctypes.byref(desc(partition_tokens=512)))
+    slots = 2 * 32 * 16
+    assert part >= slots * 16 * 128 * 4
+
+
+def _info(lib, d):
+    plan = ctypes.c_void_p()
+    assert lib.pa_plan_create(ctypes.byref(d), None, 0, ctypes.byref(plan)) == OK
+    inf = B.PlanInfo()
+    assert lib.pa_plan_get_info(plan, ctypes.byref(inf)) == OK
+    lib.pa_plan_destroy(plan)
+    return inf
+
+
+def test_shared_memory_budget_pinned(lib):
+    """The stage count and shared-memory carve are computed in one place (the plan) and
+    pinned here (ROCm/ATOM PR 2710 review, "Smaller": an unpinned mirrored LDS budget)."""
+    inf = _info(lib, desc())
+    assert inf.threads_per_cta == 288 and inf.tile_tokens == 128
+    assert inf.stages == 5 and inf.smem_bytes <= 232448
+    assert inf.grid_ctas == 152 and inf.partial_slots == 304
+    bf = _info(lib, desc(kv_dtype="bf16", scale_mode="none"))
+    assert bf.stages == 2 and bf.smem_bytes <= 232448
+    q8 = _info(lib, desc(q_len=8, q_mode="ragged", max_batch=4096))
+    assert q8.stages >= 2 and q8.smem_bytes <= 232448
+
+
+def test_create_refuses_bad_workspace(lib):
+    d = desc()
+    plan = ctypes.c_void_p()
+    assert lib.pa_plan_create(ctypes.byref(d), None, 1024, ctypes.byref(plan)) == WS
+    assert not plan.value
+    bad = desc(head_dim=96)
+    assert lib.pa_plan_create(ctypes.byref(bad), None, 0, ctypes.byref(plan)) == UNSUP
+
+
+class FakeCall:
+    """Aligned fake device addresses (never dereferenced: only pa_decode_check sees them)."""
+
+    def __init__(self, B_, rows, **over):
+        self.a = B.DecodeArgs()
+        addr = iter(range(0x100000, 0x10000000, 0x10000))
+        for f in ("q", "k_cache", "v_cache", "k_scale", "v_scale", "block_table", "context_lens",
+                  "out"):
+            setattr(self.a, f, next(addr))
+        self.a.num_pages = 4096
+        self.a.block_table_stride = 64
+        self.a.num_seqs = B_
+        self.a.num_rows = rows
+        self.a.sm_scale = 1.0 / np.sqrt(128.0)
+        self.keep = []
+        for k, v in over.items():
+            if isinstance(v, np.ndarray):
+                v = np.ascontiguousarray(v, dtype=np.int32)
+                self.keep.append(v)
+                v = v.ctypes.data
+            setattr(self.a, k, v)
+
+
+def _plan(lib, **kw):
+    d = desc(**kw)
+    plan = ctypes.c_void_p()
+    assert lib.pa_plan_create(ctypes.byref(d), None, 0, ctypes.byref(plan)) == OK
+    return plan
+
+
+def check(lib, plan, call):
+    return lib.pa_decode_check(plan, ctypes.byref(call.a))
+
+
+def test_uniform_plan_accepts_uniform_segment(lib):
+    plan = _plan(lib, q_len=4, max_batch=32, max_rows=128)
+    cu = np.arange(0, 4 * 31 + 1, 4)
+    assert check(lib, plan, FakeCall(31, 124, cu_seqlens_q_host=cu)) == OK
+    assert check(lib, plan, FakeCall(31, 124)) == OK
+
+
+def test_uniform_plan_refuses_121_rows(lib):
+    """30 requests with q_len 4 and one with q_len 1 give 121 rows, which a uniform
+    q_len-4 plan cannot hold (ROCm/ATOM PR 2122, section 2)."""
+    plan = _plan(lib, q_len=4, max_batch=32, max_rows=128)
+    assert check(lib, plan, FakeCall(31, 121)) == RAGGED
+
+
+def test_uniform_plan_refuses_4_4_6_2_with_host_mirror(lib):
+    """[4, 4, 6, 2] sums to 16 and divides by 4, yet is ragged: caught from the host
+    mirror of cu_seqlens_q (ROCm/ATOM PR 2122, section 2)."""
+    plan = _plan(lib, q_len=4, max_batch=32, max_rows=128)
+    cu = np.array([0, 4, 8, 14, 16])
+    assert check(lib, plan, FakeCall(4, 16, cu_seqlens_q_host=cu)) == RAGGED
+    assert check(lib, plan, FakeCall(4, 16, cu_seqlens_q_host=np.array([0, 4, 8, 12, 16]))) == OK
+
+
+def test_ragged_plan(lib):
+    plan = _plan(lib, q_len=8, q_mode="ragged", max_batch=32, max_rows=256)
+    cu = np.array([0, 4, 8, 14, 16])
+    assert check(lib, plan, FakeCall(4, 16)) == INVALID          # cu_seqlens_q is required
+    assert check(lib, plan, FakeCall(4, 16, cu_seqlens_q=0x9000000, cu_seqlens_q_host=cu)) == OK
+    big = np.array([0, 4, 13, 14, 16])                           # one request with 9 rows
+    assert check(lib, plan, FakeCall(4, 16, cu_seqlens_q=0x9000000, cu_seqlens_q_host=big)) == CAP
+    bad = np.array([0, 4, 3, 14, 16])
+    assert check(lib, plan, FakeCall(4, 16, cu_seqlens_q=0x9000000, cu_seqlens_q_host=bad)) == INVALID
+    wrong_total = np.array([0, 4, 8, 14, 15])
+    assert check(lib, plan, FakeCall(4, 16, cu_seqlens_q=0x9000000,
+                                      cu_seqlens_q_host=wrong_total)) == INVALID
+
+
+def test_capacity_refusals(lib):
+    plan = _plan(lib, max_batch=32, max_context_len=8192)
+    assert check(lib, plan, FakeCall(33, 33)) == CAP
+    assert check(lib, plan, FakeCall(32, 32)) == OK
+    assert check(lib, plan, FakeCall(32, 32, num_pages=1 << 30)) == CAP
+    assert check(lib, plan, FakeCall(0, 0)) == OK
+
+
+def test_pointer_and_alignment_refusals(lib):
+    plan = _plan(lib)
+    assert check(lib, plan, FakeCall(2, 2, k_scale=None)) == INVALID
+    assert check(lib, plan, FakeCall(2, 2, out=None)) == INVALID
+    assert check(lib, plan, FakeCall(2, 2, q=0x100008)) == ALIGN
+    assert check(lib, plan, FakeCall(2, 2, k_cache=0x200004)) == ALIGN
+    assert check(lib, plan, FakeCall(2, 2, sm_scale=0.0)) == INVALID
+    assert check(lib, plan, FakeCall(2, 2, sm_scale=float("nan"))) == INVALID
+    assert check(lib, plan, FakeCall(2, 2, block_table_stride=0)) == INVALID
+    assert check(lib, plan, FakeCall(2, 2, reserved0=1)) == INVALID
+
+
+def test_scalar_mode_scales(lib):
+    plan = _plan(lib, scale_mode="scalar")
+    assert check(lib, plan, FakeCall(2, 2, k_scale=None, v_scale=None, k_scale_scalar=0.01,
+                                     v_scale_scalar=0.02)) == OK
+    assert check(lib, plan, FakeCall(2, 2, k_scale_scalar=float("inf"))) == INVALID
+    assert check(lib, plan, FakeCall(2, 2, v_scale_scalar=-1.0)) == INVALID
+
+
+def test_sparse_refusals(lib):
+    dense = _plan(lib)
+    sel = dict(selected_pages=0xA000000, num_selected=0xA100000, selected_stride=64)
+    assert check(lib, dense, FakeCall(2, 2, **sel)) == UNSUP
+    sparse = _plan(lib, max_selected_pages=64)
+    assert check(lib, sparse, FakeCall(2, 2, **sel)) == OK
+    assert check(lib, sparse, FakeCall(2, 2, selected_pages=0xA000000, num_selected=0xA100000,
+                                       selected_stride=65)) == CAP
+    assert check(lib, sparse, FakeCall(2, 2, selected_pages=0xA000000, selected_stride=8)) == INVALID
+
+
+def test_decode_on_check_only_plan_launches_nothing(lib):
+    plan = _plan(lib)
+    call = FakeCall(2, 2)
+    assert lib.pa_decode(plan, ctypes.byref(call.a), None) == WS
+    rm = ctypes.c_void_p(0x7000000)
+    assert lib.pa_debug_row_map(plan, ctypes.byref(call.a), rm, None) == WS
+    assert lib.pa_debug_gather(plan, ctypes.byref(call.a), ctypes.c_void_p(0x7000000), 1 << 20,
+                               None) == WS

@@ -1,0 +1,333 @@
+"""CUDA path against the fp64 oracle, through the C ABI (needs a GPU).
+
+Bars: bf16 outputs within max-abs 1e-2 and cosine >= 0.9999 of the oracle; the row
+map and the page gather bit-exact; split-K against single pass within 1e-3 relative in
+fp32 (the tolerance of the hot path's spec).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import compare, compare_lse, rows_of, subset, SPLIT_REL
+from oracle import oracle as O
+from paged_fp8_kv_04_gb300 import device as dv
+from paged_fp8_kv_04_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def gpu_run(p, out_dtype="bf16", partition_tokens=0, plan=None, **kw):
+    d = dv.to_device(p)
+    plan = plan or dv.plan_for(p, out_dtype=out_dtype, partition_tokens=partition_tokens)
+    out, lse = dv.run(plan, p, d, lse=True, **kw)
+    torch.cuda.synchronize()
+    flags = plan.device_status()
+    return out.float().cpu().numpy(), lse.cpu().numpy(), flags
+
+
+def check_against_oracle(p, sample=None, what="", **kw):
+    out, lse, flags = gpu_run(p, **kw)
+    assert flags == 0, f"{what}: device flags {flags:#x}"
+    q = p if sample is None else subset(p, sample)
+    ref, ref_lse = O.decode(q)
+    rows = np.arange(p.num_rows) if sample is None else rows_of(p, sample)
+    compare(out[rows], ref, what)
+    compare_lse(lse[rows], ref_lse, what)
+    return out, lse
+
+
+# ------------------------------------------------------------------------ the workloads
+
+def test_tiny_dense_decode():
+    check_against_oracle(synth.tiny_dense(0), what="tiny dense")
+
+
+def test_dense_8k_full_size_sampled():
+    check_against_oracle(synth.dense_8k(1), sample=[0, 13, 31], what="dense 8K")
+
+
+def test_dense_8k_bf16_control():
+    check_against_oracle(synth.dense_8k(1, kv_dtype="bf16"), sample=[0, 31], what="bf16 control")
+
+
+@pytest.mark.parametrize("mode", ["scalar", "per_token"])
+def test_long_128k_full_size_sampled(mode):
+    check_against_oracle(synth.long_128k(2, scale_mode=mode), sample=[5], what=f"128K {mode}")
+
+
+@pytest.mark.parametrize("batch", ["A", "B"])
+def test_ragged_speculative_decode(batch):
+    p = synth.ragged_spec(3, batch)
+    if batch == "A":
+        one = int(np.flatnonzero(p.q_lens == 1)[0])
+        sample = sorted({one, (one + 1) % 31, 0})
+        assert p.num_rows == 121
+    else:
+        sample = [0, 1, 2, 3]
+        assert list(p.q_lens) == [4, 4, 6, 2]
+    check_against_oracle(p, sample=sample, what=f"ragged {batch}")
+
+
+def test_sparse_selected_pages_full_size_sampled():
+    p = synth.sparse_selected(4)
+    check_against_oracle(p, sample=[0, 7, 16, 31], what="sparse")
+
+
+# --------------------------------------------------------------------------- invariants
+
+def test_sparse_all_pages_equals_dense_on_a_slice():
+    """A slice of the sparse workload (2 requests, a real partial last page): selecting
+    every page equals the dense run; both equal the oracle."""
+    p = synth.make_problem(40, num_seqs=2, context_lens=[130000, 5000], q_lens=[1, 4],
+                           page_size=128)
+    npg = (p.context_lens + 127) // 128
+    sel = np.full((2, int(npg.max())), -1, dtype=np.int32)
+    rng = np.random.default_rng(1)
+    for r in range(2):
+        sel[r, :npg[r]] = rng.permutation(npg[r])
+    import dataclasses
+    ps = dataclasses.replace(p, selected=sel, num_selected=npg.astype(np.int32))
+    dense, _, f1 = gpu_run(p, out_dtype="f32")
+    sparse, _, f2 = gpu_run(ps, out_dtype="f32")
+    assert f1 == 0 and f2 == 0
+    scale = np.abs(dense).max()
+    assert np.abs(sparse - dense).max() <= SPLIT_REL * scale
+    ref, _ = O.decode(p)
+    compare(dense, ref, "dense slice")
+
+
+def test_split_k_matches_single_pass_fp32():
+    p = synth.long_128k(2, scale_mode="per_token", num_seqs=4)
+    single, _, f0 = gpu_run(p, out_dtype="f32", partition_tokens=1 << 20)
+    assert f0 == 0
+    scale = np.abs(single).max()
+    for part in (0, 512, 2048, 8192):
+        split, _, f = gpu_run(p, out_dtype="f32", partition_tokens=part)
+        assert f == 0
+        rel = np.abs(split - single).max() / scale
+        assert rel <= SPLIT_REL, f"partition {part}: rel {rel:.2e}"
+
+
+def test_scalar_mode_equals_uniform_per_token_scales():
+    import dataclasses
+    p = synth.make_problem(41, num_seqs=3, context_lens=[3000, 777, 129], q_lens=[1, 1, 1],
+                           scale_mode="scalar")
+    ks = np.full((p.num_pages, 1, p.page_size), np.float32(p.k_scale_scalar), np.float32)
+    vs = np.full((p.num_pages, 1, p.page_size), np.float32(p.v_scale_scalar), np.float32)
+    pt = dataclasses.replace(p, scale_mode="per_token", k_scale=ks, v_scale=vs)
+    a, _, _ = gpu_run(p, out_dtype="f32")
+    b, _, _ = gpu_run(pt, out_dtype="f32")
+    assert np.abs(a - b).max() <= SPLIT_REL * np.abs(b).max()
+
+
+def test_ragged_equals_uniform_row_by_row():
+    p = synth.make_problem(42, num_seqs=4, context_lens=[900, 4000, 300, 2500],
+                           q_lens=[4, 4, 6, 2])
+    rag, _, _ = gpu_run(p, out_dtype="f32")
+    for r in range(4):
+        one = subset(p, [r])
+        o1, _, _ = gpu_run(one, out_dtype="f32")
+        rows = rows_of(p, [r])
+        assert np.abs(rag[rows] - o1).max() <= SPLIT_REL * np.abs(o1).max()
+
+
+# ------------------------------------------------------------------------ other shapes
+
+@pytest.mark.parametrize("ps", [16, 32, 64])
+def test_page_sizes(ps):
+    p = synth.make_problem(43 + ps, num_seqs=3, context_lens=[1000, 37, 400], q_lens=[1, 1, 1],
+                           page_size=ps)
+    check_against_oracle(p, what=f"page {ps}")
+
+
+def test_two_kv_heads_ragged():
+    p = synth.make_problem(44, num_seqs=3, context_lens=[700, 260, 1500], q_lens=[2, 1, 3],
+                           num_kv_heads=2)
+    check_against_oracle(p, what="Hkv 2")
+
+
+def test_q_len_eight():
+    p = synth.make_problem(45, num_seqs=3, context_lens=[600, 128, 2049], q_lens=[8, 5, 7])
+    check_against_oracle(p, what="q_len 8")
+
+
+def test_sparse_page16_with_padding():
+    import dataclasses
+    p = synth.make_problem(46, num_seqs=3, context_lens=[1000, 300, 77], q_lens=[1, 3, 2],
+                           page_size=16, selected_pages=12)
+    sel = p.selected.copy()
+    sel[0, 3] = -1
+    p = dataclasses.replace(p, selected=sel)
+    check_against_oracle(p, what="sparse page 16")
+
+
+# ------------------------------------------------------------------------- exactness
+
+def test_row_map_bit_exact():
+    for p in (synth.ragged_spec(3, "A"), synth.ragged_spec(3, "B"), synth.tiny_dense(0)):
+        d = dv.to_device(p)
+        plan = dv.plan_for(p)
+        rm = plan.row_map(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["context_lens"],
+                          **dv.call_kwargs(p, d))
+        torch.cuda.synchronize()
+        assert np.array_equal(rm.cpu().numpy(), O.row_map(p.cu_seqlens_q, p.context_lens))
+
+
+def expected_tiles(p):
+    """Independent host listing of every KV tile: (r, h, tile, [(slot, lp, phys)])."""
+    ppt = 128 // p.page_size
+    tiles = []
+    for r in range(p.num_seqs):
+        L = int(p.context_lens[r])
+        npg = (L + p.page_size - 1) // p.page_size
+        if p.selected is None:
+            nt = (L + 127) // 128
+            lps = lambda t: [t * ppt + k if t * ppt + k < npg else -1 for k in range(ppt)]
+        else:
+            ns = int(p.num_selected[r])
+            nt = (ns + ppt - 1) // ppt
+            def lps(t, r=r, ns=ns, npg=npg):
+                out = []
+                for k in range(ppt):
+                    i = t * ppt + k
+                    e = int(p.selected[r, i]) if i < ns else -1
+                    out.append(e if 0 <= e < npg else -1)
+                return out
+        if p.q_lens[r] == 0:
+            nt = 0
+        for h in range(p.num_kv_heads):
+            for t in range(nt):
+                tiles.append((r, h, t, [(k, lp, int(p.block_table[r, lp]) if lp >= 0 else -1)
+                                        for k, lp in enumerate(lps(t))]))
+    return tiles
+
+
+@pytest.mark.parametrize("case", ["tiny", "sparse16", "ragged", "bf16", "two_heads"])
+def test_gather_bit_exact(case):
+    if case == "tiny":
+        p = synth.tiny_dense(0)
+    elif case == "sparse16":
+        p = synth.make_problem(47, num_seqs=3, context_lens=[1000, 300, 77], q_lens=[1, 3, 2],
+                               page_size=16, selected_pages=12)
+    elif case == "ragged":
+        p = synth.ragged_spec(3, "B")
+    elif case == "bf16":
+        p = synth.make_problem(48, num_seqs=2, context_lens=[300, 129], q_lens=[1, 1],
+                               kv_dtype="bf16", scale_mode="none")
+    else:
+        p = synth.make_problem(49, num_seqs=2, context_lens=[300, 129], q_lens=[1, 2],
+                               num_kv_heads=2, page_size=32)
+    tiles = expected_tiles(p)
+    d = dv.to_device(p)
+    plan = dv.plan_for(p)
+    dump, tb = plan.gather(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                           d["context_lens"], len(tiles), **dv.call_kwargs(p, d))
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    dump = dump.cpu().numpy()
+    fp8 = p.kv_dtype == "fp8"
+    rowb = 128 if fp8 else 256
+    ps = p.page_size
+    for gt, (r, h, t, slots) in enumerate(tiles):
+        blk = dump[gt * tb:(gt + 1) * tb]
+        hdr = blk[:128].view(np.int32)
+        assert (hdr[0], hdr[1], hdr[2]) == (r, h, t), (gt, hdr[:8])
+        kt = blk[128:128 + 128 * rowb].reshape(128, rowb)
+        vt = blk[128 + 128 * rowb:128 + 256 * rowb].reshape(128, rowb)
+        for k, lp, phys in slots:
+            assert hdr[16 + k] == phys and hdr[8 + k] == (lp * ps if lp >= 0 else -1)
+            if lp < 0:
+                continue
+            want_k = p.k_cache[phys, h].view(np.uint8).reshape(ps, rowb)
+            want_v = p.v_cache[phys, h].view(np.uint8).reshape(ps, rowb)
+            assert np.array_equal(kt[k * ps:(k + 1) * ps], want_k), (gt, k)
+            assert np.array_equal(vt[k * ps:(k + 1) * ps], want_v), (gt, k)
+            if fp8 and p.scale_mode == "per_token":
+                sc = blk[128 + 256 * rowb:].view(np.float32)
+                assert np.array_equal(sc[k * ps:(k + 1) * ps], p.k_scale[phys, h])
+                assert np.array_equal(sc[128 + k * ps:128 + (k + 1) * ps], p.v_scale[phys, h])
+    # the gathered positions below each request's context are, in order, the oracle's
+    # key set of the request's last row (whose cutoff is the context length)
+    for r in range(p.num_seqs):
+        if p.q_lens[r] == 0:
+            continue
+        got = []
+        for (rr, h, t, slots) in tiles:
+            if rr == r and h == 0:
+                for k, lp, phys in slots:
+                    if lp >= 0:
+                        got.extend(x for x in range(lp * ps, lp * ps + ps) if x < p.context_lens[r])
+        want = O.key_positions(p, r, int(p.q_lens[r]) - 1)
+        assert np.array_equal(np.array(got, dtype=np.int64), want), r
+
+
+# ------------------------------------------------------------------- robustness (no faults)
+
+def test_bad_page_id_is_flagged_not_read():
+    p = synth.make_problem(50, num_seqs=3, context_lens=[500, 400, 300], q_lens=[1, 1, 1])
+    bt = p.block_table.copy()
+    bt[1, 2] = p.num_pages + 5
+    import dataclasses
+    bad = dataclasses.replace(p, block_table=bt)
+    out, lse, flags = gpu_run(bad)
+    assert flags & 0x01, f"flags {flags:#x}"
+    ref, _ = O.decode(subset(p, [0, 2]))
+    compare(out[rows_of(p, [0, 2])], ref, "untouched requests")
+
+
+def test_uniform_plan_flags_ragged_device_cu():
+    """Without the host mirror, a uniform plan given the [4, 4, 6, 2] segment on the
+    device raises PA_DEV_NOT_UNIFORM instead of mis-mapping rows silently."""
+    p = synth.make_problem(51, num_seqs=4, context_lens=[300, 300, 300, 300], q_lens=[4, 4, 6, 2])
+    d = dv.to_device(p)
+    plan = dv.plan_for(p, ragged=False, q_len=4, max_context_len=300)
+    kw = dv.call_kwargs(p, d, host_mirror=False)
+    plan.decode(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["context_lens"], **kw)
+    assert plan.device_status() & 0x08
+
+
+def test_empty_key_sets_give_zeros():
+    p = synth.make_problem(52, num_seqs=3, context_lens=[0, 200, 0], q_lens=[1, 1, 1])
+    out, lse, flags = gpu_run(p)
+    assert flags & 0x04  # context_len < q_len
+    assert np.all(out[[0, 2]] == 0) and np.all(np.isneginf(lse[[0, 2]]))
+    ref, _ = O.decode(subset(p, [1]))
+    compare(out[[1]], ref, "non-empty request")
+
+
+def test_repeated_calls_bit_identical():
+    """Split-K counters reset themselves: back-to-back calls agree bit for bit."""
+    p = synth.long_128k(2, scale_mode="per_token", num_seqs=2, context=20000)
+    d = dv.to_device(p)
+    plan = dv.plan_for(p)
+    a, _ = dv.run(plan, p, d)
+    b, _ = dv.run(plan, p, d)
+    c, _ = dv.run(plan, p, d)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(b, c)
+    assert plan.device_status() == 0
+
+
+def test_cuda_graph_capture_and_replay():
+    p = synth.make_problem(53, num_seqs=4, context_lens=[5000, 3000, 7000, 100], q_lens=[1] * 4)
+    d = dv.to_device(p)
+    plan = dv.plan_for(p)
+    ref, _ = dv.run(plan, p, d)
+    out = torch.empty_like(ref)
+    kw = dv.call_kwargs(p, d)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.decode(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["context_lens"],
+                    out=out, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
