@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = balanced)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", type=int, default=0,
+                    help="only run --warmup + this many direct pa_decode calls (for ncu)")
     return ap.parse_args()
 
 
@@ -268,6 +270,15 @@ def bench_ours(args):
                                    pd["context_lens"], out=out, keep=keep, **kw))
     stream = torch.cuda.Stream(device=dev)
 
+    if args.profile:
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.profile):
+                plan.decode_args(args_list[i % npools], stream=stream)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_calls": args.warmup + args.profile,
+                          "device_flags": plan.device_status()}), flush=True)
+        return
+
     # warm-up: W direct calls
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
@@ -282,7 +293,8 @@ def bench_ours(args):
     with torch.cuda.graph(g, stream=stream):
         for i in range(chunk):
             plan.decode_args(args_list[i % npools], stream=stream)
-    g.replay()
+    with torch.cuda.stream(stream):
+        g.replay()
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local)
@@ -293,10 +305,11 @@ def bench_ours(args):
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K // chunk):
-        g.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):  # CUDAGraph.replay launches on the current stream
+        e0.record(stream)
+        for _ in range(K // chunk):
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()

@@ -68,6 +68,17 @@ enum { PA_OUT_BF16 = 0, PA_OUT_F32 = 1 };
 #define PA_DEV_TIMEOUT       0x40u  /* a bounded wait inside a kernel gave up (the output is incomplete) */
 #define PA_DEV_DUMP_RANGE    0x80u  /* pa_debug_gather's buffer was too small for the schedule */
 
+/* Plan flags.
+ * PA_PLAN_NO_PDL: launch pa_decode as an ordinary kernel.  By default it is launched
+ *   with programmatic dependent launch: its CTAs may start while the kernel before it
+ *   in the stream is finishing, and read the index inputs (block_table, context_lens,
+ *   cu_seqlens_q, selected_pages, num_selected) before that kernel has completed; they
+ *   wait for it to complete before reading q, the caches or the scales, and before
+ *   writing anything.  So with PDL on, the kernel enqueued immediately before pa_decode
+ *   must not write those index inputs (copies and host writes are unaffected).  Set
+ *   this flag if it does. */
+#define PA_PLAN_NO_PDL 0x1
+
 /* Plan descriptor: the capacity bucket and the fixed shape of every call on the plan
  * (ROCm/ATOM PR 2710 review, "Must fix" 1: size the plan by a capacity bucket).
  * Supported: head_dim 128, group_size 16, page_size in {16, 32, 64, 128},
@@ -90,7 +101,8 @@ typedef struct pa_plan_desc {
                                  else fixed split-K partitions of this many tokens (multiple of 128) */
   int32_t out_dtype;          /* PA_OUT_BF16 (round to nearest even) or PA_OUT_F32 */
   int32_t num_sms;            /* 0: the current device's SM count; > 0: use this count (sizing without a GPU) */
-  int32_t reserved[3];        /* must be 0 */
+  int32_t flags;              /* PA_PLAN_* bits */
+  int32_t reserved[2];        /* must be 0 */
 } pa_plan_desc_t;
 
 /* One decode call.  Layouts are dense row-major; rows = query tokens. */

@@ -39,8 +39,9 @@ int log2i(int x) {
 
 pa_status_t validate(const pa_plan_desc_t *d) {
   if (d == nullptr) return PA_ERR_INVALID_ARG;
-  for (int k = 0; k < 3; ++k)
+  for (int k = 0; k < 2; ++k)
     if (d->reserved[k] != 0) return PA_ERR_INVALID_ARG;
+  if ((d->flags & ~PA_PLAN_NO_PDL) != 0) return PA_ERR_INVALID_ARG;
   if (d->num_kv_heads < 1 || d->num_kv_heads > 64) return PA_ERR_UNSUPPORTED;
   if (d->group_size != pa::kG) return PA_ERR_UNSUPPORTED;
   if (d->head_dim != pa::kD) return PA_ERR_UNSUPPORTED;
@@ -131,7 +132,7 @@ pa_status_t geometry(const pa_plan_desc_t *d, Geometry *g) {
     const size_t off_bar = off;
     off += round_up((size_t)(2 * ns + 3) * 8, 16);
     const size_t off_misc = off;
-    off += 64;
+    off += pa::kMiscBytes;
     const size_t total = off + 1024;  // slack for the 1024-byte alignment of the base
     if (total <= (size_t)smem_max) {
       g->nstage = ns;
@@ -233,6 +234,8 @@ void fill_params(const pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k)
   const Geometry &g = plan->geo;
   uint8_t *ws = static_cast<uint8_t *>(plan->ws);
   k->q = static_cast<const uint16_t *>(a->q);
+  k->k_cache = static_cast<const uint8_t *>(a->k_cache);
+  k->v_cache = static_cast<const uint8_t *>(a->v_cache);
   k->k_scale = a->k_scale;
   k->v_scale = a->v_scale;
   k->block_table = a->block_table;
@@ -255,14 +258,18 @@ void fill_params(const pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k)
     k->pfold = 1.f;
     k->vpost = 1.f;
   } else if (d.scale_mode == PA_SCALE_SCALAR) {
-    // e4m3 codes widen to f16 as value * 2^-8; the 2^8 returns in the folded scales.
-    k->kfold = (float)(256.0 * (double)a->k_scale_scalar * sl2);
+    // Scalar scales: K's folds into the score scale, V's multiplies the normalised
+    // output once (vLLM PR 52060, "Suggested Fix").
+    k->kfold = (float)((double)a->k_scale_scalar * sl2);
     k->pfold = 1.f;
-    k->vpost = (float)(256.0 * (double)a->v_scale_scalar);
+    k->vpost = a->v_scale_scalar;
   } else {
-    k->kfold = (float)(256.0 * sl2);
+    // Per-token scales: k_scale[token] multiplies the score column, v_scale[token] the
+    // P column.  P' = p * v_scale * 256 keeps the f16 P operand in its normal range
+    // (v_scale ~ amax / 448); the exact power of two is undone on the output.
+    k->kfold = (float)sl2;
     k->pfold = 256.f;
-    k->vpost = 1.f;
+    k->vpost = 1.f / 256.f;
   }
   k->num_seqs = a->num_seqs;
   k->Hkv = d.num_kv_heads;
@@ -313,17 +320,27 @@ pa_status_t tensor_maps(pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k
 }
 
 template <int KVT, int SM, bool DUMP>
-cudaError_t launch_t(const pa::KParams &k, size_t smem, cudaStream_t s) {
-  pa::decode_kernel<KVT, SM, DUMP><<<k.grid, pa::kThreads, smem, s>>>(k);
-  return cudaGetLastError();
+cudaError_t launch_t(const pa::KParams &k, size_t smem, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(k.grid);
+  cfg.blockDim = dim3(pa::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, pa::decode_kernel<KVT, SM, DUMP>, k);
 }
 
 template <bool DUMP>
 cudaError_t launch(const pa_plan_desc_t &d, const pa::KParams &k, size_t smem, cudaStream_t s) {
-  if (d.kv_dtype == PA_KV_BF16) return launch_t<PA_KV_BF16, PA_SCALE_NONE, DUMP>(k, smem, s);
+  const bool pdl = (d.flags & PA_PLAN_NO_PDL) == 0;
+  if (d.kv_dtype == PA_KV_BF16) return launch_t<PA_KV_BF16, PA_SCALE_NONE, DUMP>(k, smem, s, pdl);
   if (d.scale_mode == PA_SCALE_SCALAR)
-    return launch_t<PA_KV_FP8_E4M3, PA_SCALE_SCALAR, DUMP>(k, smem, s);
-  return launch_t<PA_KV_FP8_E4M3, PA_SCALE_PER_TOKEN, DUMP>(k, smem, s);
+    return launch_t<PA_KV_FP8_E4M3, PA_SCALE_SCALAR, DUMP>(k, smem, s, pdl);
+  return launch_t<PA_KV_FP8_E4M3, PA_SCALE_PER_TOKEN, DUMP>(k, smem, s, pdl);
 }
 
 // After pa_decode_check has passed: kernel parameters for a launch.
@@ -380,7 +397,14 @@ pa_status_t pa_plan_create(const pa_plan_desc_t *desc, void *d_workspace, size_t
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaMemset(d_workspace, 0, g.off_ml) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
-    if (prepare_kernels(*desc, g.smem) != cudaSuccess) return PA_ERR_CUDA;
+    // Raise the kernels' dynamic shared-memory limit to the device maximum (not to this
+    // plan's carve), so that plans of different sizes never lower it under each other.
+    int smem_optin = 0;
+    if (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        (size_t)smem_optin < g.smem)
+      return PA_ERR_UNSUPPORTED;
+    if (prepare_kernels(*desc, (size_t)smem_optin) != cudaSuccess) return PA_ERR_CUDA;
   }
   pa_plan *p = new (std::nothrow) pa_plan;
   if (p == nullptr) return PA_ERR_INVALID_ARG;

@@ -18,6 +18,8 @@
 // The BF16 path keeps the natural d order and uses ldmatrix for its operands.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "pa_kernel.cuh"
 
 namespace pa {
@@ -100,12 +102,14 @@ __device__ __forceinline__ void reset_state(Frag &f) {
 
 // ------------------------------------------------------------------------ online softmax
 
-// s holds the log2-domain scores of this lane's 4 columns of one row; on return it
-// holds p = 2^(s - m) with m the row's running maximum.  Rescales l and the row's
+// s holds the log2-domain scores of this lane's 8 columns of one row (tokens
+// 8j + 2t + e of the chunk's n-tiles j = 0..3, column 2j + e); on return it holds
+// p = 2^(s - m) with m the row's running maximum.  Rescales l and the row's
 // accumulators (o[.][half], o[.][half + 1]) when the maximum grows.
-__device__ __forceinline__ void online_row(float (&s)[4], float &m, float &l, float (&o)[16][4],
+__device__ __forceinline__ void online_row(float (&s)[8], float &m, float &l, float (&o)[16][4],
                                            int half) {
-  float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+  float mx = fmaxf(fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3])),
+                   fmaxf(fmaxf(s[4], s[5]), fmaxf(s[6], s[7])));
   mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
   if (mx > m) {
@@ -120,135 +124,178 @@ __device__ __forceinline__ void online_row(float (&s)[4], float &m, float &l, fl
   }
   const float ref = (m == -INFINITY) ? 0.f : m;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) s[k] = fast_exp2(s[k] - ref);
-  l += (s[0] + s[1]) + (s[2] + s[3]);
+  for (int k = 0; k < 8; ++k) s[k] = fast_exp2(s[k] - ref);
+  l += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
-// Scores of the 4 columns of rows g (s0) and g + 8 (s1) -> masked -> softmax update.
-// pos0 is the position of token 2t of the chunk (or < 0 when the page slot is empty).
-__device__ __forceinline__ void mask_scores(float (&s0)[4], float (&s1)[4], int pos0, int cut) {
-  const int off[4] = {0, 1, 8, 9};
+// Masks the columns whose position is not below the row's cutoff.  pos0[h] is the
+// position of token 2t of the chunk's 16-token half h, or < 0 for an empty page slot.
+__device__ __forceinline__ void mask_scores(float (&s0)[8], float (&s1)[8], const int (&pos0)[2],
+                                            int cut) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (pos0 < 0 || pos0 + off[k] >= cut) {
+  for (int k = 0; k < 8; ++k) {
+    const int j = k >> 1, hf = j >> 1;
+    const int pos = pos0[hf] + 8 * (j & 1) + (k & 1);
+    if (pos0[hf] < 0 || pos >= cut) {
       s0[k] = -INFINITY;
       s1[k] = -INFINITY;
     }
   }
 }
 
-// --------------------------------------------------------------------- one 16-token chunk
+// P fragments of the chunk's two PV k-steps from the probabilities (per-column scale w).
+__device__ __forceinline__ void pack_p(const float (&s0)[8], const float (&s1)[8],
+                                       const float (&w)[8], bool bf16, uint32_t (&pa)[2][4]) {
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    const int c = 4 * ks;
+    if (bf16) {
+      pa[ks][0] = pack_bf16x2(s0[c] * w[c], s0[c + 1] * w[c + 1]);
+      pa[ks][1] = pack_bf16x2(s1[c] * w[c], s1[c + 1] * w[c + 1]);
+      pa[ks][2] = pack_bf16x2(s0[c + 2] * w[c + 2], s0[c + 3] * w[c + 3]);
+      pa[ks][3] = pack_bf16x2(s1[c + 2] * w[c + 2], s1[c + 3] * w[c + 3]);
+    } else {
+      pa[ks][0] = pack_f16x2(s0[c] * w[c], s0[c + 1] * w[c + 1]);
+      pa[ks][1] = pack_f16x2(s1[c] * w[c], s1[c + 1] * w[c + 1]);
+      pa[ks][2] = pack_f16x2(s0[c + 2] * w[c + 2], s0[c + 3] * w[c + 3]);
+      pa[ks][3] = pack_f16x2(s1[c + 2] * w[c + 2], s1[c + 3] * w[c + 3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------- one 32-token chunk
 
 // FP8 tile: K at st, V at st + 16384 (each [128 tokens][128 B], 128-byte swizzle),
-// K scales at st + 32768, V scales at st + 33280 (fp32 per token).
+// K scales at st + 32768, V scales at st + 33280 (fp32 per token).  Tokens tb..tb+31.
 template <int SM>
 __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb, bool masked,
-                                          int pos0, int cut, int g, int t, Frag &f) {
+                                          const int (&pos0)[2], int cut, int g, int t, Frag &f) {
   const uint32_t Kb = st, Vb = st + 16384;
   const uint32_t sw0 = ((2 * t) ^ g) << 4, sw1 = ((2 * t + 1) ^ g) << 4;
-  const uint4 ka0 = lds128(Kb + (tb + g) * 128 + sw0), ka1 = lds128(Kb + (tb + g) * 128 + sw1);
-  const uint4 kb0 = lds128(Kb + (tb + 8 + g) * 128 + sw0);
-  const uint4 kb1 = lds128(Kb + (tb + 8 + g) * 128 + sw1);
-  const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-  const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t w[4][8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t rb = Kb + (tb + 8 * j + g) * 128;
+    const uint4 x = lds128(rb + sw0), y = lds128(rb + sw1);
+    w[j][0] = x.x; w[j][1] = x.y; w[j][2] = x.z; w[j][3] = x.w;
+    w[j][4] = y.x; w[j][5] = y.y; w[j][6] = y.z; w[j][7] = y.w;
+  }
+  float acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    uint32_t b0, b1, c0, c1;
-    e4m3x4_to_f16x2x2(wa[kk], b0, b1);
-    e4m3x4_to_f16x2x2(wb[kk], c0, c1);
-    mma_f16(sa, f.qf[kk], b0, b1);
-    mma_f16(sb, f.qf[kk], c0, c1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t b0, b1;
+      e4m3x4_to_f16x2x2(w[j][kk], b0, b1);
+      mma_f16(acc[j], f.qf[kk], b0, b1);
+    }
   }
-  float k0, k1, k2, k3;
+  float c[8], vw[8];
   if (SM == PA_SCALE_PER_TOKEN) {
-    const float2 x = lds64f(st + 32768 + (tb + 2 * t) * 4);
-    const float2 y = lds64f(st + 32768 + (tb + 8 + 2 * t) * 4);
-    k0 = x.x * p.kfold;
-    k1 = x.y * p.kfold;
-    k2 = y.x * p.kfold;
-    k3 = y.y * p.kfold;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = lds64f(st + 32768 + (tb + 8 * j + 2 * t) * 4);
+      const float2 y = lds64f(st + 33280 + (tb + 8 * j + 2 * t) * 4);
+      c[2 * j] = x.x * p.kfold;
+      c[2 * j + 1] = x.y * p.kfold;
+      vw[2 * j] = y.x * p.pfold;
+      vw[2 * j + 1] = y.y * p.pfold;
+    }
   } else {
-    k0 = k1 = k2 = k3 = p.kfold;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      c[k] = p.kfold;
+      vw[k] = 1.f;
+    }
   }
-  float s0[4] = {sa[0] * k0, sa[1] * k1, sb[0] * k2, sb[1] * k3};
-  float s1[4] = {sa[2] * k0, sa[3] * k1, sb[2] * k2, sb[3] * k3};
+  float s0[8], s1[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    s0[2 * j] = acc[j][0] * c[2 * j];
+    s0[2 * j + 1] = acc[j][1] * c[2 * j + 1];
+    s1[2 * j] = acc[j][2] * c[2 * j];
+    s1[2 * j + 1] = acc[j][3] * c[2 * j + 1];
+  }
   if (masked) mask_scores(s0, s1, pos0, cut);
   online_row(s0, f.m[0], f.l[0], f.o, 0);
   online_row(s1, f.m[1], f.l[1], f.o, 2);
-  uint32_t pa[4];
-  if (SM == PA_SCALE_PER_TOKEN) {
-    const float2 x = lds64f(st + 33280 + (tb + 2 * t) * 4);
-    const float2 y = lds64f(st + 33280 + (tb + 8 + 2 * t) * 4);
-    const float w0 = x.x * p.pfold, w1 = x.y * p.pfold, w2 = y.x * p.pfold, w3 = y.y * p.pfold;
-    pa[0] = pack_f16x2(s0[0] * w0, s0[1] * w1);
-    pa[1] = pack_f16x2(s1[0] * w0, s1[1] * w1);
-    pa[2] = pack_f16x2(s0[2] * w2, s0[3] * w3);
-    pa[3] = pack_f16x2(s1[2] * w2, s1[3] * w3);
-  } else {
-    pa[0] = pack_f16x2(s0[0], s0[1]);
-    pa[1] = pack_f16x2(s1[0], s1[1]);
-    pa[2] = pack_f16x2(s0[2], s0[3]);
-    pa[3] = pack_f16x2(s1[2], s1[3]);
-  }
-  const int rv = tb + 2 * t;
-  const uint32_t sv0 = (g ^ (2 * t)) << 4, sv1 = (g ^ (2 * t + 1)) << 4;
-  const uint4 va = lds128(Vb + rv * 128 + sv0), vb = lds128(Vb + (rv + 1) * 128 + sv1);
-  const uint4 vc = lds128(Vb + (rv + 8) * 128 + sv0), vd = lds128(Vb + (rv + 9) * 128 + sv1);
-  const uint32_t A[4] = {va.x, va.y, va.z, va.w}, Bw[4] = {vb.x, vb.y, vb.z, vb.w};
-  const uint32_t C[4] = {vc.x, vc.y, vc.z, vc.w}, Dw[4] = {vd.x, vd.y, vd.z, vd.w};
+  uint32_t pa[2][4];
+  pack_p(s0, s1, vw, false, pa);
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    uint32_t x0, x1, y0, y1;
-    e4m3x4_to_f16x2x2(prmt(A[w], Bw[w], 0x5140), x0, x1);
-    e4m3x4_to_f16x2x2(prmt(C[w], Dw[w], 0x5140), y0, y1);
-    mma_f16(f.o[4 * w], pa, x0, y0);
-    mma_f16(f.o[4 * w + 1], pa, x1, y1);
-    e4m3x4_to_f16x2x2(prmt(A[w], Bw[w], 0x7362), x0, x1);
-    e4m3x4_to_f16x2x2(prmt(C[w], Dw[w], 0x7362), y0, y1);
-    mma_f16(f.o[4 * w + 2], pa, x0, y0);
-    mma_f16(f.o[4 * w + 3], pa, x1, y1);
+  for (int ks = 0; ks < 2; ++ks) {
+    const int rv = tb + 16 * ks + 2 * t;
+    const uint32_t sv0 = (g ^ (2 * t)) << 4, sv1 = (g ^ (2 * t + 1)) << 4;
+    const uint4 va = lds128(Vb + rv * 128 + sv0), vb = lds128(Vb + (rv + 1) * 128 + sv1);
+    const uint4 vc = lds128(Vb + (rv + 8) * 128 + sv0), vd = lds128(Vb + (rv + 9) * 128 + sv1);
+    const uint32_t A[4] = {va.x, va.y, va.z, va.w}, Bw[4] = {vb.x, vb.y, vb.z, vb.w};
+    const uint32_t C[4] = {vc.x, vc.y, vc.z, vc.w}, Dw[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t x0, x1, y0, y1;
+      e4m3x4_to_f16x2x2(prmt(A[q], Bw[q], 0x5140), x0, x1);
+      e4m3x4_to_f16x2x2(prmt(C[q], Dw[q], 0x5140), y0, y1);
+      mma_f16(f.o[4 * q], pa[ks], x0, y0);
+      mma_f16(f.o[4 * q + 1], pa[ks], x1, y1);
+      e4m3x4_to_f16x2x2(prmt(A[q], Bw[q], 0x7362), x0, x1);
+      e4m3x4_to_f16x2x2(prmt(C[q], Dw[q], 0x7362), y0, y1);
+      mma_f16(f.o[4 * q + 2], pa[ks], x0, y0);
+      mma_f16(f.o[4 * q + 3], pa[ks], x1, y1);
+    }
   }
 }
 
 // BF16 tile: K halves (d 0-63, 64-127) at st and st + 16384, V halves at st + 32768 and
-// st + 49152, each [128 tokens][128 B] with 128-byte swizzle.
+// st + 49152, each [128 tokens][128 B] with 128-byte swizzle.  Tokens tb..tb+31.
 __device__ __forceinline__ void chunk_bf16(const KParams &p, uint32_t st, int tb, bool masked,
-                                           int pos0, int cut, int g, int t, int lane, Frag &f) {
+                                           const int (&pos0)[2], int cut, int g, int t, int lane,
+                                           Frag &f) {
   const int mat = lane >> 3, rr = lane & 7;
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-  {
-    const int row = tb + 8 * (mat >> 1) + rr;
+  float acc[4][4];
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int c16 = 2 * kk + (mat & 1);
+  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int c16 = 2 * kk + (mat & 1);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int row = tb + 8 * (2 * q + (mat >> 1)) + rr;
       const uint32_t addr = st + (c16 >> 3) * 16384 + row * 128 + (((c16 & 7) ^ rr) << 4);
       uint32_t r0, r1, r2, r3;
       ldsm_x4(addr, r0, r1, r2, r3);
-      mma_bf16(sa, f.qf[kk], r0, r1);
-      mma_bf16(sb, f.qf[kk], r2, r3);
+      mma_bf16(acc[2 * q], f.qf[kk], r0, r1);
+      mma_bf16(acc[2 * q + 1], f.qf[kk], r2, r3);
     }
   }
   const float k = p.kfold;
-  float s0[4] = {sa[0] * k, sa[1] * k, sb[0] * k, sb[1] * k};
-  float s1[4] = {sa[2] * k, sa[3] * k, sb[2] * k, sb[3] * k};
+  float s0[8], s1[8], vw[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    s0[2 * j] = acc[j][0] * k;
+    s0[2 * j + 1] = acc[j][1] * k;
+    s1[2 * j] = acc[j][2] * k;
+    s1[2 * j + 1] = acc[j][3] * k;
+    vw[2 * j] = vw[2 * j + 1] = 1.f;
+  }
   if (masked) mask_scores(s0, s1, pos0, cut);
   online_row(s0, f.m[0], f.l[0], f.o, 0);
   online_row(s1, f.m[1], f.l[1], f.o, 2);
-  uint32_t pa[4];
-  pa[0] = pack_bf16x2(s0[0], s0[1]);
-  pa[1] = pack_bf16x2(s1[0], s1[1]);
-  pa[2] = pack_bf16x2(s0[2], s0[3]);
-  pa[3] = pack_bf16x2(s1[2], s1[3]);
-  const int tok = tb + 8 * (mat & 1) + rr;
+  uint32_t pa[2][4];
+  pack_p(s0, s1, vw, true, pa);
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    const int c16 = j + (mat >> 1);
-    const uint32_t addr = st + 32768 + (c16 >> 3) * 16384 + tok * 128 + (((c16 & 7) ^ rr) << 4);
-    uint32_t r0, r1, r2, r3;
-    ldsm_x4_t(addr, r0, r1, r2, r3);
-    mma_bf16(f.o[j], pa, r0, r1);
-    mma_bf16(f.o[j + 1], pa, r2, r3);
+  for (int ks = 0; ks < 2; ++ks) {
+    const int tok = tb + 16 * ks + 8 * (mat & 1) + rr;
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const int c16 = j + (mat >> 1);
+      const uint32_t addr =
+          st + 32768 + (c16 >> 3) * 16384 + tok * 128 + (((c16 & 7) ^ rr) << 4);
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_t(addr, r0, r1, r2, r3);
+      mma_bf16(f.o[j], pa[ks], r0, r1);
+      mma_bf16(f.o[j + 1], pa[ks], r2, r3);
+    }
   }
 }
 
@@ -347,58 +394,122 @@ __device__ __forceinline__ void write_final(const KParams &p, const Frag &f, int
   }
 }
 
-// Split-K partial of one m-tile: m, l per row and the unnormalised o in natural d order.
-template <int KVT>
+// Split-K partial of one m-tile: m, l per row, and the unnormalised accumulators in
+// fragment order ([m-tile][i][lane][4] float4s: one coalesced 512-byte store per i).
 __device__ __forceinline__ void write_partial(const KParams &p, const Frag &f, int slot,
-                                              int mtile, int g, int t) {
+                                              int mtile, int g, int t, int lane) {
+  float4 *dst = reinterpret_cast<float4 *>(p.part_o) +
+                ((int64_t)slot * (p.mmax / kG) + mtile) * (16 * 32) + lane;
 #pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    const float lq = quad_sum(f.l[hf]);
-    const int rowi = mtile * kG + g + 8 * hf;
-    if (t == 0) {
-      p.part_ml[((int64_t)slot * 2) * p.mmax + rowi] = f.m[hf];
-      p.part_ml[((int64_t)slot * 2 + 1) * p.mmax + rowi] = lq;
-    }
-    float *dst = p.part_o + ((int64_t)slot * p.mmax + rowi) * kD;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      dst[dmap<KVT>(i, 0, t)] = f.o[i][2 * hf];
-      dst[dmap<KVT>(i, 1, t)] = f.o[i][2 * hf + 1];
-    }
+  for (int i = 0; i < 16; ++i)
+    __stcg(dst + i * 32, make_float4(f.o[i][0], f.o[i][1], f.o[i][2], f.o[i][3]));
+  // (m_g, m_g+8, l_g, l_g+8) of the row pair of lane group g: one float4 per pair.
+  const float lq0 = quad_sum(f.l[0]), lq1 = quad_sum(f.l[1]);
+  if (t == 0)
+    __stcg(reinterpret_cast<float4 *>(p.part_ml) + ((int64_t)slot * (p.mmax / kG) + mtile) * 8 + g,
+           make_float4(f.m[0], f.m[1], lq0, lq1));
+}
+
+// Stores one unit of a merged fragment: rows g and g + 8 of query token `tok`, the two
+// head-dim columns of accumulator index i for lane (g, t).
+template <int KVT>
+__device__ __forceinline__ void store_unit(const KParams &p, int tok, int head0, int i, int g,
+                                           int t, float4 v, float s0, float s1) {
+  const int Hq = p.Hkv * kG;
+  const int d0 = dmap<KVT>(i, 0, t), d1 = dmap<KVT>(i, 1, t);
+  const int64_t e0 = ((int64_t)tok * Hq + head0 + g) * kD, e1 = e0 + 8 * kD;
+  if (p.out_f32) {
+    float *o = static_cast<float *>(p.out);
+    o[e0 + d0] = v.x * s0;
+    o[e0 + d1] = v.y * s0;
+    o[e1 + d0] = v.z * s1;
+    o[e1 + d1] = v.w * s1;
+  } else {
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out);
+    o[e0 + d0] = __float2bfloat16_rn(v.x * s0);
+    o[e0 + d1] = __float2bfloat16_rn(v.y * s0);
+    o[e1 + d0] = __float2bfloat16_rn(v.z * s1);
+    o[e1 + d1] = __float2bfloat16_rn(v.w * s1);
   }
 }
 
 // The last CTA to finish a split sequence merges every partial (log-sum-exp merge).
-__device__ void merge_partials(const KParams &p, int r, int h, int row0, int qlen, int c_first,
-                               int n, int ctid) {
-  const int rows = qlen * kG, Hq = p.Hkv * kG;
-  for (int u = ctid; u < rows * 32; u += kNCW * 32) {
-    const int row = u >> 5, d4 = u & 31;
-    float M = -INFINITY;
-    for (int k = 0; k < n; ++k) {
-      const int sl = slot_of(c_first + k, c_first);
-      M = fmaxf(M, __ldcg(p.part_ml + ((int64_t)sl * 2) * p.mmax + row));
+// Lane-thread u handles fragment units u and u + 256 of an m-tile, which belong to the
+// same two rows, so one batch of independent loads brings the maxima, sums and
+// accumulators of up to 8 partials: one memory round trip per 8 partials.
+template <int KVT>
+__device__ void merge_partials(const KParams &p, int h, int row0, int qlen, int c_first, int n,
+                               int ctid) {
+  const int units = qlen * kG * 32;
+  const float4 *src = reinterpret_cast<const float4 *>(p.part_o);
+  const int64_t slot_f4 = (int64_t)(p.mmax / kG) * 512;  // float4s per partial slot
+  for (int ub = (ctid & 255); ub < units; ub += 512) {
+    const int u1 = ub + 256;  // same m-tile, same lane, accumulator index + 8
+    const int mt = ub >> 9, ln = ub & 31, gg = ln >> 2, tt = ln & 3;
+    const int r0w = mt * kG + gg;
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    for (int k0 = 0; k0 < n; k0 += 8) {
+      float m0[8], m1[8], l0[8], l1[8];
+      float4 v0[8], v1[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (k0 + j < n) {
+          const int64_t sl = slot_of(c_first + k0 + j, c_first);
+          const float4 ml = __ldcg(reinterpret_cast<const float4 *>(p.part_ml) +
+                                   (sl * (p.mmax / kG) + mt) * 8 + gg);
+          m0[j] = ml.x;
+          m1[j] = ml.y;
+          l0[j] = ml.z;
+          l1[j] = ml.w;
+          v0[j] = __ldcg(src + sl * slot_f4 + ub);
+          v1[j] = __ldcg(src + sl * slot_f4 + u1);
+        } else {
+          m0[j] = m1[j] = -INFINITY;
+          l0[j] = l1[j] = 0.f;
+          v0[j] = v1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float n0 = M0, n1 = M1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        n0 = fmaxf(n0, m0[j]);
+        n1 = fmaxf(n1, m1[j]);
+      }
+      const float c0 = n0 == -INFINITY ? 0.f : fast_exp2(M0 - n0);
+      const float c1 = n1 == -INFINITY ? 0.f : fast_exp2(M1 - n1);
+      a0.x *= c0; a0.y *= c0; a0.z *= c1; a0.w *= c1;
+      a1.x *= c0; a1.y *= c0; a1.z *= c1; a1.w *= c1;
+      L0 *= c0;
+      L1 *= c1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w0 = n0 == -INFINITY ? 0.f : fast_exp2(m0[j] - n0);
+        const float w1 = n1 == -INFINITY ? 0.f : fast_exp2(m1[j] - n1);
+        a0.x += w0 * v0[j].x; a0.y += w0 * v0[j].y; a0.z += w1 * v0[j].z; a0.w += w1 * v0[j].w;
+        a1.x += w0 * v1[j].x; a1.y += w0 * v1[j].y; a1.z += w1 * v1[j].z; a1.w += w1 * v1[j].w;
+        L0 += w0 * l0[j];
+        L1 += w1 * l1[j];
+      }
+      M0 = n0;
+      M1 = n1;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float Ls = 0.f;
-    for (int k = 0; k < n; ++k) {
-      const int sl = slot_of(c_first + k, c_first);
-      const float mm = __ldcg(p.part_ml + ((int64_t)sl * 2) * p.mmax + row);
-      const float w = (mm == -INFINITY) ? 0.f : fast_exp2(mm - M);
-      Ls += w * __ldcg(p.part_ml + ((int64_t)sl * 2 + 1) * p.mmax + row);
-      const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part_o + ((int64_t)sl * p.mmax + row) * kD) + d4);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+    const float s0 = L0 > 0.f ? p.vpost / L0 : 0.f, s1 = L1 > 0.f ? p.vpost / L1 : 0.f;
+    const int i0 = (ub >> 5) & 15;
+    store_unit<KVT>(p, row0 + mt, h * kG, i0, gg, tt, a0, s0, s1);
+    store_unit<KVT>(p, row0 + mt, h * kG, i0 + 8, gg, tt, a1, s0, s1);
+    if (i0 == 0 && tt == 0 && p.lse != nullptr) {
+      float *lp = p.lse + (int64_t)(row0 + mt) * (p.Hkv * kG) + h * kG + gg;
+      lp[0] = L0 > 0.f ? (M0 + log2f(L0)) * kLn2 : -INFINITY;
+      lp[8] = L1 > 0.f ? (M1 + log2f(L1)) * kLn2 : -INFINITY;
     }
-    const float sc = Ls > 0.f ? p.vpost / Ls : 0.f;
-    const float v[4] = {acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc};
-    const int orow = row0 + (row >> 4), head = h * kG + (row & 15);
-    store_out(p, ((int64_t)orow * Hq + head) * kD + 4 * d4, v, 4);
-    if (d4 == 0 && p.lse != nullptr)
-      p.lse[(int64_t)orow * Hq + head] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
   }
+}
+
+// Merges several exchange slots (k0 .. k0 + cnt - 1) into this warp's state.
+__device__ __forceinline__ void merge_states(const Smem &sm, int k0, int cnt, int stride, Frag &f,
+                                             int lane) {
+  for (int j = 0; j < cnt; ++j) merge_state(sm, k0 + j * stride, f, lane);
 }
 
 }  // namespace pa

@@ -72,11 +72,16 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
 
   Frag f;
   reset_state(f);
-  int mt = 1, ts = kNCW, mtile = 0, slice = 0, cut = 0;
-  bool active = false;
+  // Warp -> work map of the current request (fixed at its first tile):
+  //  q_len <= 4: two groups of 4 warps take alternate tiles (warps 0-3 even, 4-7 odd);
+  //              in a group, m-tile = query token, and 4 / q_len token slices per tile;
+  //  q_len  > 4: every warp takes every tile, one m-tile (query token) per warp.
+  int mt = 1, ts = 1, nsl = 1, mtile = 0, sub = 0, slice = 0, cut = 0;
+  bool active = false, paired = true;
   const int tile_bytes = (KVT == PA_KV_FP8_E4M3) ? (kDumpHeader + 2 * kTile * kD + 1024)
                                                   : (kDumpHeader + 4 * kTile * kD);
   const int n = b - a;
+  bool has_head = false, has_tail = false;  // split sequences (records in misc[])
   for (int i = 0; i < n; ++i) {
     const int s = i % p.nstage;
     if (!mbar_wait_bounded(sm.full(s), (i / p.nstage) & 1)) {
@@ -88,10 +93,22 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     const int qlen = meta->qlen, row0 = meta->row0, L = meta->L;
     if (flags & F_BEGIN) {
       mt = qlen;
-      ts = kNCW / mt;
-      active = warp < mt * ts;
-      mtile = warp % mt;
-      slice = warp / mt;
+      paired = mt <= 4;
+      if (paired) {
+        const int wl = warp & 3;
+        ts = 4 / mt;
+        active = wl < mt * ts;
+        mtile = wl % mt;
+        sub = wl / mt;
+        slice = (warp >> 2) * ts + sub;
+        nsl = 2 * ts;
+      } else {
+        ts = 1;
+        active = warp < mt;
+        mtile = warp % mt;
+        sub = slice = 0;
+        nsl = 1;
+      }
       cut = L - qlen + mtile + 1;
       if (!DUMP && active) {
         load_q<KVT>(p, sm.qslot(meta->qslot) + mtile * kQRowBytes, g, t, f);
@@ -100,17 +117,22 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.qempty(meta->qslot));
     }
+    const bool mine = active && (!paired || (i & 1) == (warp >> 2));
     if (DUMP) {
       dump_stage<KVT, SM>(p, sm, s, ctid, tile_bytes);
-    } else if (active) {
+    } else if (mine) {
       const bool masked = (flags & F_MASK) != 0;
       const int tps = kTile / ts;
       const uint32_t st = sm.stage(s);
-      for (int tb = slice * tps; tb < (slice + 1) * tps; tb += 16) {
-        int pos0 = 0;
+      for (int tb = sub * tps; tb < (sub + 1) * tps; tb += 32) {
+        int pos0[2] = {0, 0};
         if (masked) {
-          const int pp = meta->page_pos[tb >> p.ps_shift];
-          pos0 = pp < 0 ? -1 : pp + (tb & (p.ps - 1)) + 2 * t;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int tk = tb + 16 * hf;
+            const int pp = meta->page_pos[tk >> p.ps_shift];
+            pos0[hf] = pp < 0 ? -1 : pp + (tk & (p.ps - 1)) + 2 * t;
+          }
         }
         if (KVT == PA_KV_FP8_E4M3)
           chunk_fp8<SM>(p, st, tb, masked, pos0, cut, g, t, f);
@@ -124,34 +146,87 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     if (DUMP || !(flags & F_END)) continue;
 
     // ---- end of this CTA's part of sequence (r, h): merge the token slices -----------
-    for (int step = ts >> 1; step >= 1; step >>= 1) {
-      if (active && slice >= step && slice < 2 * step) put_state(sm, (slice - step) * mt + mtile, f, lane);
-      cons_sync(p, sm, cphase);
-      if (active && slice < step) merge_state(sm, slice * mt + mtile, f, lane);
-      cons_sync(p, sm, cphase);
+    // Pairs of slices while more than 4 remain, then all remaining into slice 0, so the
+    // exchange buffer (4 slots) is never exceeded: 8 slices take two rounds.
+    for (int cnt = nsl; cnt > 1;) {
+      if (cnt > 4 || (cnt - 1) * mt > 4) {
+        const int half = cnt >> 1;
+        if (active && slice >= half && slice < cnt) put_state(sm, (slice - half) * mt + mtile, f, lane);
+        cons_sync(p, sm, cphase);
+        if (active && slice < half) merge_state(sm, slice * mt + mtile, f, lane);
+        cons_sync(p, sm, cphase);
+        cnt = half;
+      } else {
+        if (active && slice >= 1 && slice < cnt) put_state(sm, (slice - 1) * mt + mtile, f, lane);
+        cons_sync(p, sm, cphase);
+        if (active && slice == 0) merge_states(sm, mtile, cnt - 1, mt, f, lane);
+        cons_sync(p, sm, cphase);
+        cnt = 1;
+      }
     }
     const bool writer = active && slice == 0;
     if (flags & F_WHOLE) {
       if (writer) write_final<KVT>(p, f, row0 + mtile, h * kG, g, t);
       continue;
     }
+    // A split sequence: store this CTA's partial.  If the sequence ends before the CTA's
+    // last tile it is the one the CTA started in the middle of: its writers count the
+    // arrival at once (the other warps stream on), so that its merge falls to one of
+    // the sequence's other CTAs.  The sequence the CTA leaves unfinished is counted
+    // after the last tile.
     const int nt = tstart[r + 1] - tstart[r];
     const int gs = tstart[r] * p.Hkv + h * nt;
     int c_first, nc;
     seq_ctas(p, tstart, r, h, gs, gs + nt, c_first, nc);
-    if (writer) write_partial<KVT>(p, f, slot_of(blockIdx.x, c_first), mtile, g, t);
+    if (writer) write_partial(p, f, slot_of(blockIdx.x, c_first), mtile, g, t, lane);
+    const bool is_head = i < n - 1;
+    if (ctid == 0) {
+      int32_t *rec = sm.misc() + (is_head ? M_HEAD : M_TAIL);
+      rec[0] = r;
+      rec[1] = h;
+      rec[2] = row0;
+      rec[3] = qlen;
+      rec[4] = c_first;
+      rec[5] = nc;
+    }
+    if (is_head) {
+      has_head = true;
+      if (writer) {
+        __threadfence();
+        if (lane == 0) {
+          const int w = atomicAdd(&sm.misc()[M_WCNT], 1);
+          if (w == mt - 1) {
+            sm.misc()[M_WCNT] = 0;
+            const int old = atomicAdd(p.counters + (r * p.Hkv + h), 1);
+            sm.misc()[M_LAST] = (old == nc - 1) ? 1 : 0;
+          }
+        }
+      }
+    } else {
+      has_tail = true;
+    }
+  }
+
+  if (DUMP || !(has_head || has_tail)) return;
+  if (has_tail) {
     __threadfence();
     cons_sync(p, sm, cphase);
     if (ctid == 0) {
-      const int old = atomicAdd(p.counters + (r * p.Hkv + h), 1);
-      sm.misc()[M_LAST] = (old == nc - 1) ? 1 : 0;
+      const int32_t *rec = sm.misc() + M_TAIL;
+      const int old = atomicAdd(p.counters + (rec[0] * p.Hkv + rec[1]), 1);
+      sm.misc()[M_LAST + 1] = (old == rec[5] - 1) ? 1 : 0;
     }
-    cons_sync(p, sm, cphase);
-    if (sm.misc()[M_LAST]) {
-      __threadfence();
-      merge_partials(p, r, h, row0, qlen, c_first, nc, ctid);
-      if (ctid == 0) p.counters[r * p.Hkv + h] = 0;
-    }
+  }
+  cons_sync(p, sm, cphase);
+#pragma unroll 1
+  for (int k = 0; k < 2; ++k) {
+    const bool mine_k = k == 0 ? has_head : has_tail;
+    if (!mine_k || !sm.misc()[M_LAST + k]) continue;
+    const int32_t *rec = sm.misc() + (k == 0 ? M_HEAD : M_TAIL);
+    const int rr = rec[0], hh = rec[1];
+    __threadfence();
+    merge_partials<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], ctid);
+    if (ctid == 0) p.counters[rr * p.Hkv + hh] = 0;
   }
 }
 
@@ -159,7 +234,7 @@ template <int KVT, int SM, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t mis = smem_u32(smem_raw) & 1023u;
-  Smem sm{smem_raw + ((1024u - mis) & 1023u), &p};
+  const Smem sm = Smem::make(smem_raw + ((1024u - mis) & 1023u), p);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.nstage; ++s) {
@@ -171,15 +246,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(sm.consbar(), kNCW);
     sm.misc()[M_ABORT] = 0;
     sm.misc()[M_LAST] = 0;
+    sm.misc()[M_LAST + 1] = 0;
+    sm.misc()[M_WCNT] = 0;
     fence_barrier_init();
   }
-  scan_tiles(p, sm.tstart(), sm.misc() + M_WSUM, blockIdx.x == 0);
+  pdl_launch_dependents();
+  const uint32_t fl = scan_tiles(p, sm.tstart(), sm.misc() + M_WSUM);
+  const uint32_t report = blockIdx.x == 0 ? fl : 0u;
   int a, b;
   cta_range(p, sm.tstart(), blockIdx.x, a, b);
   if (warp == kNCW) {
-    if (a < b) run_producer<KVT, SM>(p, sm, a, b);
+    // The producer reads index inputs before the wait, q and the caches after it.
+    if (a < b) run_producer<KVT, SM>(p, sm, a, b, report);
+    else {
+      pdl_wait();
+      if (report) atomicOr(p.status, report);
+    }
     return;
   }
+  pdl_wait();  // consumers write outputs and the workspace
+  if (report) atomicOr(p.status, report);
   run_consumer<KVT, SM, DUMP>(p, sm, a, b, warp, lane);
 }
 

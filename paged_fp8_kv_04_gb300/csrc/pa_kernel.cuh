@@ -57,6 +57,7 @@ struct KParams {
   CUtensorMap tm_k;               // 2-D map over [num_pages * Hkv * page_size rows, row bytes]
   CUtensorMap tm_v;
   const uint16_t *q;
+  const uint8_t *k_cache, *v_cache;  // for L2 prefetch of upcoming pages
   const float *k_scale, *v_scale;
   const int32_t *block_table, *context_lens, *cu_q, *sel, *nsel;
   void *out;
@@ -123,7 +124,8 @@ __device__ __forceinline__ ReqInfo request_info(const KParams &p, int r, uint32_
 }
 
 // Exclusive prefix of tile counts over requests into tstart[0..B] (shared memory).
-__device__ void scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum, bool report) {
+// Returns this thread's PA_DEV_* flags (reported once the kernel may write).
+__device__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.num_seqs;
   const int per = (B + kThreads - 1) / kThreads;
@@ -159,8 +161,8 @@ __device__ void scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum, boo
     tstart[r] = run;
     run += n;
   }
-  if (report && fl) atomicOr(p.status, fl);
   __syncthreads();
+  return fl;
 }
 
 // Global tile index -> (request, KV head, tile within the request's head).
@@ -221,29 +223,47 @@ __device__ __forceinline__ int slot_of(int c, int c_first) { return c == c_first
 
 // --------------------------------------------------------------------- shared-memory map
 
+// Shared-memory map: every address is computed once at kernel entry and kept in
+// registers (no reads of the parameter block inside the loops).
 struct Smem {
-  uint8_t *base;
-  const KParams *p;
-  __device__ uint32_t stage(int s) const { return smem_u32(base) + s * p->stage_bytes; }
-  __device__ uint32_t qslot(int k) const { return smem_u32(base) + p->off_q + k * p->qslot_bytes; }
-  __device__ uint32_t merge() const { return smem_u32(base) + p->off_merge; }
-  __device__ int32_t *tstart() const { return reinterpret_cast<int32_t *>(base + p->off_tstart); }
-  __device__ StageMeta *meta(int s) const {
-    return reinterpret_cast<StageMeta *>(base + p->off_meta) + s;
+  uint8_t *base;           // generic pointer to the 1024-aligned base
+  uint32_t sb;             // its shared-window address
+  uint32_t stage_bytes, nstage, q0, qslot_bytes, merge_a, bar0;
+  int32_t *tstart_p, *misc_p;
+  StageMeta *meta_p;
+  __device__ static Smem make(uint8_t *b, const KParams &p) {
+    Smem m;
+    m.base = b;
+    m.sb = smem_u32(b);
+    m.stage_bytes = p.stage_bytes;
+    m.nstage = p.nstage;
+    m.q0 = m.sb + p.off_q;
+    m.qslot_bytes = p.qslot_bytes;
+    m.merge_a = m.sb + p.off_merge;
+    m.bar0 = m.sb + p.off_bar;
+    m.tstart_p = reinterpret_cast<int32_t *>(b + p.off_tstart);
+    m.misc_p = reinterpret_cast<int32_t *>(b + p.off_misc);
+    m.meta_p = reinterpret_cast<StageMeta *>(b + p.off_meta);
+    return m;
   }
-  __device__ uint32_t full(int s) const { return smem_u32(base) + p->off_bar + 8 * s; }
-  __device__ uint32_t empty(int s) const {
-    return smem_u32(base) + p->off_bar + 8 * (p->nstage + s);
-  }
-  __device__ uint32_t qempty(int k) const {
-    return smem_u32(base) + p->off_bar + 8 * (2 * p->nstage + k);
-  }
-  __device__ uint32_t consbar() const { return smem_u32(base) + p->off_bar + 8 * (2 * p->nstage + 2); }
-  __device__ int32_t *misc() const { return reinterpret_cast<int32_t *>(base + p->off_misc); }
+  __device__ uint32_t stage(int s) const { return sb + s * stage_bytes; }
+  __device__ uint32_t qslot(int k) const { return q0 + k * qslot_bytes; }
+  __device__ uint32_t merge() const { return merge_a; }
+  __device__ int32_t *tstart() const { return tstart_p; }
+  __device__ StageMeta *meta(int s) const { return meta_p + s; }
+  __device__ uint32_t full(int s) const { return bar0 + 8 * s; }
+  __device__ uint32_t empty(int s) const { return bar0 + 8 * (nstage + s); }
+  __device__ uint32_t qempty(int k) const { return bar0 + 8 * (2 * nstage + k); }
+  __device__ uint32_t consbar() const { return bar0 + 8 * (2 * nstage + 2); }
+  __device__ int32_t *misc() const { return misc_p; }
 };
 
 // misc[] words
-enum : int { M_ABORT = 0, M_LAST = 1, M_WSUM = 4 };  // M_WSUM.. holds 9 warp sums
+// M_LAST, M_LAST + 1: merge duty for the head / tail sequence; M_WCNT: writer warps that
+// have stored their part of the head partial; M_WSUM..: 9 warp sums of the prologue scan.
+// M_HEAD, M_TAIL: (request, head, first row, q_len, first CTA, CTA count) of each.
+enum : int { M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24 };
+constexpr int kMiscBytes = 128;
 
 __device__ __forceinline__ void raise_flag(const KParams &p, const Smem &sm, uint32_t f) {
   atomicOr(p.status, f);

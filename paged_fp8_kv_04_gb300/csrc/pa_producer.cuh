@@ -20,7 +20,7 @@ __device__ __forceinline__ uint32_t page_bytes(int ps) {
 // TMA copies (K and V rows with 128-byte swizzle, per-token scales, and the
 // request's query rows at the first tile of a request).
 template <int KVT, int SM>
-__device__ void run_producer(const KParams &p, const Smem &sm, int a, int b) {
+__device__ void run_producer(const KParams &p, const Smem &sm, int a, int b, uint32_t report) {
   const int lane = threadIdx.x & 31;
   const int ppt = p.ppt, nb = 32 / ppt;
   const int slot = lane / ppt, kpg = lane - slot * ppt;
@@ -29,7 +29,7 @@ __device__ void run_producer(const KParams &p, const Smem &sm, int a, int b) {
   const uint64_t pol = l2_evict_first_policy();
   const uint32_t pbytes = page_bytes<KVT, SM>(ps);
   int i = 0, seg = 0;
-  bool ok = true;
+  bool ok = true, waited_deps = false;
 
   for (int base = a; base < b && ok; base += nb) {
     const int gt = base + slot;
@@ -64,6 +64,13 @@ __device__ void run_producer(const KParams &p, const Smem &sm, int a, int b) {
           pos = lp * ps;
         }
       }
+    }
+    if (!waited_deps) {
+      // Everything above read only index inputs; q, the caches, the scales and the
+      // workspace wait for the kernels this launch depends on.
+      pdl_wait();
+      waited_deps = true;
+      if (report) atomicOr(p.status, report);
     }
     if (fl) atomicOr(p.status, fl);
     const unsigned valid_bits = __ballot_sync(~0u, phys >= 0);
@@ -140,6 +147,22 @@ __device__ void run_producer(const KParams &p, const Smem &sm, int a, int b) {
           tma_load_2d(st + 16384 + po, &p.tm_k, 64, row, fb, pol);
           tma_load_2d(st + 32768 + po, &p.tm_v, 0, row, fb, pol);
           tma_load_2d(st + 49152 + po, &p.tm_v, 64, row, fb, pol);
+        }
+      }
+      // L2 prefetch of the pages of tile j + nstage, whose TMA copy is issued once tile j
+      // is released: the copy then finds its bytes in L2 instead of waiting on HBM.
+      {
+        const int jp = j + p.nstage;
+        const int ph_src = jp * ppt;
+        if (jp < nbat && lane >= ph_src && lane < ph_src + ppt && phys >= 0) {
+          const int32_t rowp = (phys * p.Hkv + h) * ps;
+          const uint32_t rb = (KVT == PA_KV_FP8_E4M3 ? 1u : 2u) * kD;
+          prefetch_l2(p.k_cache + (int64_t)rowp * rb, ps * rb);
+          prefetch_l2(p.v_cache + (int64_t)rowp * rb, ps * rb);
+          if (SM == PA_SCALE_PER_TOKEN) {
+            prefetch_l2(p.k_scale + rowp, ps * 4);
+            prefetch_l2(p.v_scale + rowp, ps * 4);
+          }
         }
       }
       if (begin && lane < qj) {

@@ -120,6 +120,19 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, ui
       : "memory");
 }
 
+// Warm L2 with a contiguous range (16-B aligned, size a multiple of 16); no completion.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its CTAs, and
+// wait until the kernels this one depends on have completed (both are no-ops when the
+// launch has no programmatic dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------------ tensor cores
 
 // D = A * B + D, m16n8k16, f16 inputs, f32 accumulators.

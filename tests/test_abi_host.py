@@ -68,6 +68,10 @@ def test_reserved_fields_must_be_zero(lib):
     d = desc()
     d.reserved[1] = 3
     assert lib.pa_plan_validate(ctypes.byref(d)) == INVALID
+    d = desc()
+    d.flags = 0x4
+    assert lib.pa_plan_validate(ctypes.byref(d)) == INVALID
+    assert lib.pa_plan_validate(ctypes.byref(desc(pdl=False))) == OK
 
 
 def test_workspace_size_is_bounded_and_deterministic(lib):
