@@ -190,6 +190,32 @@ void pa_plan_destroy(pa_plan_t *plan);
 /* A static string naming the status. */
 const char *pa_status_string(pa_status_t status);
 
+/* Size of the fixed device scratch that pa_decode_noalloc uses (8 MiB per GPU). */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* pa_decode for callers that cannot allocate device memory when they set up or run a
+ * decode -- for example an engine plugin whose enqueue step must not allocate, or a
+ * runtime whose device memory pool is fixed before the first request -- and so cannot
+ * hand pa_plan_create a workspace.  No source page has a counterpart of this call: it
+ * is a convenience of this library.
+ *
+ * It takes the plan descriptor directly and runs the same decode as pa_decode, with the
+ * split-K scratch in one fixed array of PA_NOALLOC_SCRATCH_BYTES that the library
+ * reserves on every GPU that loads it, for the life of the process.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine, host or device.
+ *  - Descriptors whose workspace (pa_plan_workspace_size) exceeds the array are
+ *    refused with PA_ERR_CAPACITY (on 152 SMs a balanced plan fits for q_len <= 3);
+ *    other refusals are those of pa_plan_create and pa_decode_check.
+ *  - The first call on a device looks up the array's device address and sets the
+ *    kernels' shared-memory limit for that device; make that first call before any
+ *    stream capture on the device.
+ *  - Each call first clears the scratch's status word and arrival counters on `stream`.
+ *    All calls on a device share the one array, so calls that may overlap on the GPU
+ *    (different streams without ordering between them) race and corrupt each other.
+ *  - Device-side data flags (PA_DEV_*) of these calls are not reported. */
+pa_status_t pa_decode_noalloc(const pa_plan_desc_t *desc, const pa_decode_args_t *args,
+                              void *stream);
+
 /* ---- test hooks: exact integer / byte outputs of the row map and the page gather ---- */
 
 /* For every query row: (request, query token, causal cutoff) as int32 triples into the

@@ -108,6 +108,8 @@ def lib(path: Optional[str] = None):
     L.pa_debug_gather_tile_bytes.restype = ctypes.c_size_t
     L.pa_debug_gather.argtypes = [P, ctypes.POINTER(DecodeArgs), P, ctypes.c_size_t, P]
     L.pa_debug_gather.restype = ctypes.c_int
+    L.pa_decode_noalloc.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(DecodeArgs), P]
+    L.pa_decode_noalloc.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <new>
 
@@ -548,3 +549,79 @@ pa_status_t pa_debug_gather(pa_plan_t *plan, const pa_decode_args_t *args, void 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// Decode without a caller-provided workspace.  The split-K scratch (status word, arrival
+// counters, partial maxima, sums and accumulators) lives in one fixed device array that
+// this library defines; every GPU that loads the library holds it until the process
+// exits.  See pa_decode_noalloc in pa.h.
+
+namespace {
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+  std::once_flag once;
+  void *ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Once per device, with that device current: the device address of the scratch array
+// (its name in host code is only a stand-in) and the kernels' shared-memory limit.
+void noalloc_setup(NoAllocDevice &nd) {
+  void *ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  int dev = 0, smem_optin = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  pa_plan_desc_t d;
+  std::memset(&d, 0, sizeof(d));
+  const int modes[3][2] = {{PA_KV_FP8_E4M3, PA_SCALE_PER_TOKEN},
+                           {PA_KV_FP8_E4M3, PA_SCALE_SCALAR},
+                           {PA_KV_BF16, PA_SCALE_NONE}};
+  for (int m = 0; m < 3 && e == cudaSuccess; ++m) {
+    d.kv_dtype = modes[m][0];
+    d.scale_mode = modes[m][1];
+    e = prepare_kernels(d, (size_t)smem_optin);
+  }
+  nd.ptr = ptr;
+  nd.err = e;
+}
+
+}  // namespace
+
+extern "C" pa_status_t pa_decode_noalloc(const pa_plan_desc_t *desc, const pa_decode_args_t *args,
+                                         void *stream) {
+  if (desc == nullptr || args == nullptr) return PA_ERR_INVALID_ARG;
+  Geometry g;
+  pa_status_t st = geometry(desc, &g);
+  if (st != PA_OK) return st;
+  if (g.ws > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_CAPACITY;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PA_ERR_UNSUPPORTED;
+  NoAllocDevice &nd = g_noalloc_dev[dev];
+  std::call_once(nd.once, noalloc_setup, std::ref(nd));
+  if (nd.err != cudaSuccess || nd.ptr == nullptr) return PA_ERR_CUDA;
+
+  pa_plan plan;  // on the stack: no host or device allocation
+  plan.desc = *desc;
+  plan.geo = g;
+  plan.device = dev;
+  plan.ws = nd.ptr;
+  if ((st = pa_decode_check(&plan, args)) != PA_OK) return st;
+  if (args->num_seqs == 0) return PA_OK;
+  // The status word and the arrival counters must start at zero; the rest of the
+  // scratch is written before it is read.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(nd.ptr, 0, g.off_ml, s) != cudaSuccess) return PA_ERR_CUDA;
+  pa::KParams k;
+  std::memset(&k, 0, sizeof(k));
+  if ((st = prepare_call(&plan, args, &k)) != PA_OK) return st;
+  if (launch<false>(plan.desc, k, g.smem, s) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}

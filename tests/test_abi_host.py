@@ -237,3 +237,13 @@ def test_decode_on_check_only_plan_launches_nothing(lib):
     assert lib.pa_debug_row_map(plan, ctypes.byref(call.a), rm, None) == WS
     assert lib.pa_debug_gather(plan, ctypes.byref(call.a), ctypes.c_void_p(0x7000000), 1 << 20,
                                None) == WS
+
+
+def test_noalloc_refuses_a_plan_larger_than_its_scratch(lib):
+    """pa_decode_noalloc refuses, before touching a GPU, a descriptor whose workspace
+    exceeds its fixed scratch (q_len 8 on 152 SMs needs about 20 MB)."""
+    big = desc(q_len=8, q_mode="ragged")
+    assert lib.pa_plan_workspace_size(ctypes.byref(big)) > (8 << 20)
+    call = FakeCall(2, 2, cu_seqlens_q=0x9000000)
+    assert lib.pa_decode_noalloc(ctypes.byref(big), ctypes.byref(call.a), None) == CAP
+    assert lib.pa_decode_noalloc(None, ctypes.byref(call.a), None) == INVALID
