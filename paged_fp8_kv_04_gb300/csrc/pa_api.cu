@@ -209,8 +209,14 @@ struct pa_plan {
 
 namespace {
 
+// Also checks the build's register count: the kernel's register split assumes the
+// launch allocation of exactly kLaunchRegs per thread (any other count is refused).
 template <int KVT, int SM, bool DUMP>
 cudaError_t set_smem_attr(size_t smem) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, pa::decode_kernel<KVT, SM, DUMP>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != pa::kLaunchRegs) return cudaErrorInvalidKernelImage;
   return cudaFuncSetAttribute(pa::decode_kernel<KVT, SM, DUMP>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }

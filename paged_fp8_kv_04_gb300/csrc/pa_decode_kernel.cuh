@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const uint32_t report = blockIdx.x == 0 ? fl : 0u;
   int a, b;
   cta_range(p, sm.tstart(), blockIdx.x, a, b);
-  if (warp == kNCW) {
+  if (warp >= kNCW) {
+    regs_dec<kProdRegs>();
+    if (warp != kNCW) return;  // the rest of the producer warpgroup only gives registers
     // The producer reads index inputs before the wait, q and the caches after it.
     if (a < b) run_producer<KVT, SM>(p, sm, a, b, report);
     else {
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     return;
   }
+  regs_inc<kConsRegs>();
   pdl_wait();  // consumers write outputs and the workspace
   if (report) atomicOr(p.status, report);
   run_consumer<KVT, SM, DUMP>(p, sm, a, b, warp, lane);

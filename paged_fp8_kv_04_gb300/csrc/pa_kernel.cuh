@@ -33,8 +33,16 @@ namespace pa {
 constexpr int kD = 128;          // head_dim
 constexpr int kG = 16;           // query heads per KV head (rows of one m-tile)
 constexpr int kTile = 128;       // tokens per KV tile
-constexpr int kNCW = 8;          // consumer warps
-constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kNCW = 8;          // consumer warps (two warpgroups)
+constexpr int kThreads = (kNCW + 4) * 32;  // + one producer warpgroup (warp kNCW copies)
+// Register split: the CTA is launched at kLaunchRegs per thread; the producer warpgroup
+// gives registers back down to kProdRegs and the consumer warpgroups take kConsRegs.
+// Both totals agree, per CTA and per SM sub-partition (each holds one warp of each
+// warpgroup), so the consumers' increase is always satisfied.  The host refuses to
+// launch a build whose register count is not kLaunchRegs.
+constexpr int kLaunchRegs = 168, kProdRegs = 56, kConsRegs = 224;
+static_assert(kNCW * 32 * kConsRegs + 4 * 32 * kProdRegs == kThreads * kLaunchRegs,
+              "register split must match the launch allocation");
 constexpr int kMaxQ = 8;         // most query tokens per request (m-tiles)
 constexpr int kQRowBytes = kG * kD * 2;   // one query token's 16 heads, bf16
 constexpr int kMergeBytes = 4 * 8192 + 4 * 512;
@@ -260,7 +268,7 @@ struct Smem {
 
 // misc[] words
 // M_LAST, M_LAST + 1: merge duty for the head / tail sequence; M_WCNT: writer warps that
-// have stored their part of the head partial; M_WSUM..: 9 warp sums of the prologue scan.
+// have stored their part of the head partial; M_WSUM..: 12 warp sums of the prologue scan.
 // M_HEAD, M_TAIL: (request, head, first row, q_len, first CTA, CTA count) of each.
 enum : int { M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24 };
 constexpr int kMiscBytes = 128;

@@ -101,7 +101,7 @@ def test_shared_memory_budget_pinned(lib):
     """The stage count and shared-memory carve are computed in one place (the plan) and
     pinned here (ROCm/ATOM PR 2710 review, "Smaller": an unpinned mirrored LDS budget)."""
     inf = _info(lib, desc())
-    assert inf.threads_per_cta == 288 and inf.tile_tokens == 128
+    assert inf.threads_per_cta == 384 and inf.tile_tokens == 128
     assert inf.stages == 5 and inf.smem_bytes <= 232448
     assert inf.grid_ctas == 152 and inf.partial_slots == 304
     bf = _info(lib, desc(kv_dtype="bf16", scale_mode="none"))
