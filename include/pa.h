@@ -78,6 +78,13 @@ enum { PA_OUT_BF16 = 0, PA_OUT_F32 = 1 };
  *   must not write those index inputs (copies and host writes are unaffected).  Set
  *   this flag if it does. */
 #define PA_PLAN_NO_PDL 0x1
+/* PA_PLAN_TCGEN05: for an FP8 plan with q_len 1, run the tcgen05 kernel, which feeds the
+ *   cache bytes to the tensor core (QK^T and PV as kind::f8f6f4 MMAs with accumulators
+ *   in tensor memory), instead of the default mma.sync kernel, which widens e4m3 to f16
+ *   on the SM sub-partitions.  Both give the same results within the library's
+ *   tolerances.  On GB300 the default kernel is currently the faster of the two; the
+ *   flag is ignored for other plans. */
+#define PA_PLAN_TCGEN05 0x2
 
 /* Plan descriptor: the capacity bucket and the fixed shape of every call on the plan
  * (ROCm/ATOM PR 2710 review, "Must fix" 1: size the plan by a capacity bucket).

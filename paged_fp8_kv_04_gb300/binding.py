@@ -20,6 +20,7 @@ SCALE_NONE, SCALE_SCALAR, SCALE_PER_TOKEN = 0, 1, 2
 Q_UNIFORM, Q_RAGGED = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 PLAN_NO_PDL = 0x1
+PLAN_TCGEN05 = 0x2
 
 STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CAPACITY",
           4: "PA_ERR_RAGGED", 5: "PA_ERR_ALIGN", 6: "PA_ERR_CUDA", 7: "PA_ERR_DEVICE_DATA",
@@ -118,7 +119,7 @@ def lib(path: Optional[str] = None):
 def make_desc(*, num_kv_heads=1, group_size=16, head_dim=128, page_size=128, kv_dtype="fp8",
               scale_mode="per_token", q_mode="uniform", q_len=1, max_batch=1, max_rows=None,
               max_context_len=1, max_selected_pages=0, partition_tokens=0, out_dtype="bf16",
-              num_sms=0, pdl=True) -> PlanDesc:
+              num_sms=0, pdl=True, tcgen05=False) -> PlanDesc:
     d = PlanDesc()
     d.num_kv_heads, d.group_size, d.head_dim, d.page_size = num_kv_heads, group_size, head_dim, page_size
     d.kv_dtype = {"fp8": KV_FP8_E4M3, "bf16": KV_BF16}[kv_dtype] if isinstance(kv_dtype, str) else kv_dtype
@@ -131,7 +132,7 @@ def make_desc(*, num_kv_heads=1, group_size=16, head_dim=128, page_size=128, kv_
     d.partition_tokens = partition_tokens
     d.out_dtype = {"bf16": OUT_BF16, "f32": OUT_F32}[out_dtype] if isinstance(out_dtype, str) else out_dtype
     d.num_sms = num_sms
-    d.flags = 0 if pdl else PLAN_NO_PDL
+    d.flags = (0 if pdl else PLAN_NO_PDL) | (PLAN_TCGEN05 if tcgen05 else 0)
     return d
 
 

@@ -15,6 +15,7 @@
 
 #include "pa.h"
 #include "pa_decode_kernel.cuh"
+#include "pa_umma.cuh"
 
 namespace {
 
@@ -42,7 +43,7 @@ pa_status_t validate(const pa_plan_desc_t *d) {
   if (d == nullptr) return PA_ERR_INVALID_ARG;
   for (int k = 0; k < 2; ++k)
     if (d->reserved[k] != 0) return PA_ERR_INVALID_ARG;
-  if ((d->flags & ~PA_PLAN_NO_PDL) != 0) return PA_ERR_INVALID_ARG;
+  if ((d->flags & ~(PA_PLAN_NO_PDL | PA_PLAN_TCGEN05)) != 0) return PA_ERR_INVALID_ARG;
   if (d->num_kv_heads < 1 || d->num_kv_heads > 64) return PA_ERR_UNSUPPORTED;
   if (d->group_size != pa::kG) return PA_ERR_UNSUPPORTED;
   if (d->head_dim != pa::kD) return PA_ERR_UNSUPPORTED;
@@ -131,7 +132,7 @@ pa_status_t geometry(const pa_plan_desc_t *d, Geometry *g) {
     const size_t off_meta = off;
     off += (size_t)ns * sizeof(pa::StageMeta);
     const size_t off_bar = off;
-    off += round_up((size_t)(2 * ns + 3) * 8, 16);
+    off += round_up((size_t)(2 * ns + 3 + pa::kUmmaBars) * 8, 16);
     const size_t off_misc = off;
     off += pa::kMiscBytes;
     const size_t total = off + 1024;  // slack for the 1024-byte alignment of the base
@@ -221,8 +222,28 @@ cudaError_t set_smem_attr(size_t smem) {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
+// The tcgen05 kernel serves FP8 plans whose requests have one query token, on request.
+bool use_umma(const pa_plan_desc_t &d) {
+  return d.kv_dtype == PA_KV_FP8_E4M3 && d.q_len == 1 && (d.flags & PA_PLAN_TCGEN05) != 0;
+}
+
+template <int SM>
+cudaError_t set_umma_attr(size_t smem) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, pa::decode_umma_kernel<SM>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != pa::kLaunchRegs) return cudaErrorInvalidKernelImage;
+  return cudaFuncSetAttribute(pa::decode_umma_kernel<SM>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
 cudaError_t prepare_kernels(const pa_plan_desc_t &d, size_t smem) {
   cudaError_t e;
+  if (use_umma(d)) {
+    e = d.scale_mode == PA_SCALE_SCALAR ? set_umma_attr<PA_SCALE_SCALAR>(smem)
+                                        : set_umma_attr<PA_SCALE_PER_TOKEN>(smem);
+    if (e != cudaSuccess) return e;
+  }
   if (d.kv_dtype == PA_KV_BF16) {
     if ((e = set_smem_attr<PA_KV_BF16, PA_SCALE_NONE, false>(smem)) != cudaSuccess) return e;
     return set_smem_attr<PA_KV_BF16, PA_SCALE_NONE, true>(smem);
@@ -341,9 +362,32 @@ cudaError_t launch_t(const pa::KParams &k, size_t smem, cudaStream_t s, bool pdl
   return cudaLaunchKernelEx(&cfg, pa::decode_kernel<KVT, SM, DUMP>, k);
 }
 
+template <int SM>
+cudaError_t launch_umma(const pa::KParams &k, size_t smem, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(k.grid);
+  cfg.blockDim = dim3(pa::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  pa::KParams ku = k;
+  // The tcgen05 kernel folds the per-token V scale into P relative to its maximum and
+  // undoes the 256 of P's range itself: only the scalar V scale is left for the end.
+  if (SM == PA_SCALE_PER_TOKEN) ku.vpost = 1.f;
+  return cudaLaunchKernelEx(&cfg, pa::decode_umma_kernel<SM>, ku);
+}
+
 template <bool DUMP>
 cudaError_t launch(const pa_plan_desc_t &d, const pa::KParams &k, size_t smem, cudaStream_t s) {
   const bool pdl = (d.flags & PA_PLAN_NO_PDL) == 0;
+  if (!DUMP && use_umma(d)) {
+    if (d.scale_mode == PA_SCALE_SCALAR) return launch_umma<PA_SCALE_SCALAR>(k, smem, s, pdl);
+    return launch_umma<PA_SCALE_PER_TOKEN>(k, smem, s, pdl);
+  }
   if (d.kv_dtype == PA_KV_BF16) return launch_t<PA_KV_BF16, PA_SCALE_NONE, DUMP>(k, smem, s, pdl);
   if (d.scale_mode == PA_SCALE_SCALAR)
     return launch_t<PA_KV_FP8_E4M3, PA_SCALE_SCALAR, DUMP>(k, smem, s, pdl);

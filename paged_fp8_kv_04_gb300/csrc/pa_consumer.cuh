@@ -106,10 +106,12 @@ __device__ __forceinline__ void reset_state(Frag &f) {
 // 8j + 2t + e of the chunk's n-tiles j = 0..3, column 2j + e); on return it holds
 // p = 2^(s - m) with m the row's running maximum.  Rescales l and the row's
 // accumulators (o[.][half], o[.][half + 1]) when the maximum grows.
-__device__ __forceinline__ void online_row(float (&s)[8], float &m, float &l, float (&o)[16][4],
+template <int N>
+__device__ __forceinline__ void online_row(float (&s)[N], float &m, float &l, float (&o)[16][4],
                                            int half) {
-  float mx = fmaxf(fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3])),
-                   fmaxf(fmaxf(s[4], s[5]), fmaxf(s[6], s[7])));
+  float mx = s[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) mx = fmaxf(mx, s[k]);
   mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
   if (mx > m) {
@@ -124,16 +126,20 @@ __device__ __forceinline__ void online_row(float (&s)[8], float &m, float &l, fl
   }
   const float ref = (m == -INFINITY) ? 0.f : m;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) s[k] = fast_exp2(s[k] - ref);
-  l += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+  for (int k = 0; k < N; ++k) s[k] = fast_exp2(s[k] - ref);
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; k += 4) sum += (s[k] + s[k + 1]) + (s[k + 2] + s[k + 3]);
+  l += sum;
 }
 
 // Masks the columns whose position is not below the row's cutoff.  pos0[h] is the
 // position of token 2t of the chunk's 16-token half h, or < 0 for an empty page slot.
-__device__ __forceinline__ void mask_scores(float (&s0)[8], float (&s1)[8], const int (&pos0)[2],
-                                            int cut) {
+template <int N>
+__device__ __forceinline__ void mask_scores(float (&s0)[N], float (&s1)[N],
+                                            const int (&pos0)[N / 4], int cut) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < N; ++k) {
     const int j = k >> 1, hf = j >> 1;
     const int pos = pos0[hf] + 8 * (j & 1) + (k & 1);
     if (pos0[hf] < 0 || pos >= cut) {
@@ -144,10 +150,11 @@ __device__ __forceinline__ void mask_scores(float (&s0)[8], float (&s1)[8], cons
 }
 
 // P fragments of the chunk's two PV k-steps from the probabilities (per-column scale w).
-__device__ __forceinline__ void pack_p(const float (&s0)[8], const float (&s1)[8],
-                                       const float (&w)[8], bool bf16, uint32_t (&pa)[2][4]) {
+template <int N>
+__device__ __forceinline__ void pack_p(const float (&s0)[N], const float (&s1)[N],
+                                       const float (&w)[N], bool bf16, uint32_t (&pa)[N / 4][4]) {
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
+  for (int ks = 0; ks < N / 4; ++ks) {
     const int c = 4 * ks;
     if (bf16) {
       pa[ks][0] = pack_bf16x2(s0[c] * w[c], s0[c + 1] * w[c + 1]);
@@ -163,39 +170,43 @@ __device__ __forceinline__ void pack_p(const float (&s0)[8], const float (&s1)[8
   }
 }
 
-// ---------------------------------------------------------------------- one 32-token chunk
+// ---------------------------------------------------------------- 32 or 64-token chunks
 
 // FP8 tile: K at st, V at st + 16384 (each [128 tokens][128 B], 128-byte swizzle),
-// K scales at st + 32768, V scales at st + 33280 (fp32 per token).  Tokens tb..tb+31.
-template <int SM>
+// K scales at st + 32768, V scales at st + 33280 (fp32 per token).  Tokens tb ..
+// tb + 32 NCH - 1.  With NCH = 2 the warp holds two independent chains per step (8 QK
+// n-tiles, 4 PV k-steps), which keeps the tensor and conversion pipes busier per warp.
+template <int SM, int NCH>
 __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb, bool masked,
-                                          const int (&pos0)[2], int cut, int g, int t, Frag &f) {
+                                          const int (&pos0)[2 * NCH], int cut, int Lctx, int g,
+                                          int t, Frag &f) {
+  constexpr int NJ = 4 * NCH, NC = 2 * NJ, NKS = 2 * NCH;
   const uint32_t Kb = st, Vb = st + 16384;
   const uint32_t sw0 = ((2 * t) ^ g) << 4, sw1 = ((2 * t + 1) ^ g) << 4;
-  uint32_t w[4][8];
+  uint32_t w[NJ][8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < NJ; ++j) {
     const uint32_t rb = Kb + (tb + 8 * j + g) * 128;
     const uint4 x = lds128(rb + sw0), y = lds128(rb + sw1);
     w[j][0] = x.x; w[j][1] = x.y; w[j][2] = x.z; w[j][3] = x.w;
     w[j][4] = y.x; w[j][5] = y.y; w[j][6] = y.z; w[j][7] = y.w;
   }
-  float acc[4][4];
+  float acc[NJ][4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  for (int j = 0; j < NJ; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NJ; ++j) {
       uint32_t b0, b1;
       e4m3x4_to_f16x2x2(w[j][kk], b0, b1);
       mma_f16(acc[j], f.qf[kk], b0, b1);
     }
   }
-  float c[8], vw[8];
+  float c[NC], vw[NC];
   if (SM == PA_SCALE_PER_TOKEN) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < NJ; ++j) {
       const float2 x = lds64f(st + 32768 + (tb + 8 * j + 2 * t) * 4);
       const float2 y = lds64f(st + 33280 + (tb + 8 * j + 2 * t) * 4);
       c[2 * j] = x.x * p.kfold;
@@ -205,30 +216,40 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < NC; ++k) {
       c[k] = p.kfold;
       vw[k] = 1.f;
     }
   }
-  float s0[8], s1[8];
+  float s0[NC], s1[NC];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < NJ; ++j) {
     s0[2 * j] = acc[j][0] * c[2 * j];
     s0[2 * j + 1] = acc[j][1] * c[2 * j + 1];
     s1[2 * j] = acc[j][2] * c[2 * j];
     s1[2 * j + 1] = acc[j][3] * c[2 * j + 1];
   }
-  if (masked) mask_scores(s0, s1, pos0, cut);
-  online_row(s0, f.m[0], f.l[0], f.o, 0);
-  online_row(s1, f.m[1], f.l[1], f.o, 2);
-  uint32_t pa[2][4];
-  pack_p(s0, s1, vw, false, pa);
+  if (masked) mask_scores<NC>(s0, s1, pos0, cut);
+  online_row<NC>(s0, f.m[0], f.l[0], f.o, 0);
+  online_row<NC>(s1, f.m[1], f.l[1], f.o, 2);
+  uint32_t pa[NKS][4];
+  pack_p<NC>(s0, s1, vw, false, pa);
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
+  for (int ks = 0; ks < NKS; ++ks) {
     const int rv = tb + 16 * ks + 2 * t;
     const uint32_t sv0 = (g ^ (2 * t)) << 4, sv1 = (g ^ (2 * t + 1)) << 4;
-    const uint4 va = lds128(Vb + rv * 128 + sv0), vb = lds128(Vb + (rv + 1) * 128 + sv1);
-    const uint4 vc = lds128(Vb + (rv + 8) * 128 + sv0), vd = lds128(Vb + (rv + 9) * 128 + sv1);
+    uint4 va = lds128(Vb + rv * 128 + sv0), vb = lds128(Vb + (rv + 1) * 128 + sv1);
+    uint4 vc = lds128(Vb + (rv + 8) * 128 + sv0), vd = lds128(Vb + (rv + 9) * 128 + sv1);
+    if (masked) {
+      // Slots past the context or of an empty page may hold any bytes, NaN codes
+      // included, and 0 * NaN = NaN: their V rows enter the product as zeros.
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const int pk = pos0[ks];
+      if (pk < 0 || pk >= Lctx) va = z;
+      if (pk < 0 || pk + 1 >= Lctx) vb = z;
+      if (pk < 0 || pk + 8 >= Lctx) vc = z;
+      if (pk < 0 || pk + 9 >= Lctx) vd = z;
+    }
     const uint32_t A[4] = {va.x, va.y, va.z, va.w}, Bw[4] = {vb.x, vb.y, vb.z, vb.w};
     const uint32_t C[4] = {vc.x, vc.y, vc.z, vc.w}, Dw[4] = {vd.x, vd.y, vd.z, vd.w};
 #pragma unroll
@@ -249,7 +270,8 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
 // BF16 tile: K halves (d 0-63, 64-127) at st and st + 16384, V halves at st + 32768 and
 // st + 49152, each [128 tokens][128 B] with 128-byte swizzle.  Tokens tb..tb+31.
 __device__ __forceinline__ void chunk_bf16(const KParams &p, uint32_t st, int tb, bool masked,
-                                           const int (&pos0)[2], int cut, int g, int t, int lane,
+                                           const int (&pos0)[2], int cut, const int32_t *page_pos,
+                                           int Lctx, uint32_t zline, int g, int t, int lane,
                                            Frag &f) {
   const int mat = lane >> 3, rr = lane & 7;
   float acc[4][4];
@@ -278,19 +300,24 @@ __device__ __forceinline__ void chunk_bf16(const KParams &p, uint32_t st, int tb
     s1[2 * j + 1] = acc[j][3] * k;
     vw[2 * j] = vw[2 * j + 1] = 1.f;
   }
-  if (masked) mask_scores(s0, s1, pos0, cut);
-  online_row(s0, f.m[0], f.l[0], f.o, 0);
-  online_row(s1, f.m[1], f.l[1], f.o, 2);
+  if (masked) mask_scores<8>(s0, s1, pos0, cut);
+  online_row<8>(s0, f.m[0], f.l[0], f.o, 0);
+  online_row<8>(s1, f.m[1], f.l[1], f.o, 2);
   uint32_t pa[2][4];
-  pack_p(s0, s1, vw, true, pa);
+  pack_p<8>(s0, s1, vw, true, pa);
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     const int tok = tb + 16 * ks + 8 * (mat & 1) + rr;
+    bool dead = false;  // a slot past the context or of an empty page: read a zero line
+    if (masked) {
+      const int pp = page_pos[tok >> p.ps_shift];
+      dead = pp < 0 || pp + (tok & (p.ps - 1)) >= Lctx;
+    }
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
       const int c16 = j + (mat >> 1);
       const uint32_t addr =
-          st + 32768 + (c16 >> 3) * 16384 + tok * 128 + (((c16 & 7) ^ rr) << 4);
+          dead ? zline : st + 32768 + (c16 >> 3) * 16384 + tok * 128 + (((c16 & 7) ^ rr) << 4);
       uint32_t r0, r1, r2, r3;
       ldsm_x4_t(addr, r0, r1, r2, r3);
       mma_bf16(f.o[j], pa[ks], r0, r1);

@@ -77,7 +77,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
   //              in a group, m-tile = query token, and 4 / q_len token slices per tile;
   //  q_len  > 4: every warp takes every tile, one m-tile (query token) per warp.
   int mt = 1, ts = 1, nsl = 1, mtile = 0, sub = 0, slice = 0, cut = 0;
-  bool active = false, paired = true;
+  bool active = false, paired = true, quad = false;
   const int tile_bytes = (KVT == PA_KV_FP8_E4M3) ? (kDumpHeader + 2 * kTile * kD + 1024)
                                                   : (kDumpHeader + 4 * kTile * kD);
   const int n = b - a;
@@ -94,7 +94,17 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     if (flags & F_BEGIN) {
       mt = qlen;
       paired = mt <= 4;
-      if (paired) {
+      // FP8 with one query token: four groups of two warps take every fourth tile, each
+      // warp a 64-token half (two independent chains per step).
+      quad = KVT == PA_KV_FP8_E4M3 && mt == 1;
+      if (quad) {
+        ts = 2;
+        active = true;
+        mtile = 0;
+        sub = warp & 1;
+        slice = warp;  // (group, half) = (warp >> 1, warp & 1)
+        nsl = 8;
+      } else if (paired) {
         const int wl = warp & 3;
         ts = 4 / mt;
         active = wl < mt * ts;
@@ -117,27 +127,41 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.qempty(meta->qslot));
     }
-    const bool mine = active && (!paired || (i & 1) == (warp >> 2));
+    const bool mine = active && (quad ? (i & 3) == (warp >> 1) : (!paired || (i & 1) == (warp >> 2)));
     if (DUMP) {
       dump_stage<KVT, SM>(p, sm, s, ctid, tile_bytes);
     } else if (mine) {
       const bool masked = (flags & F_MASK) != 0;
       const int tps = kTile / ts;
       const uint32_t st = sm.stage(s);
-      for (int tb = sub * tps; tb < (sub + 1) * tps; tb += 32) {
-        int pos0[2] = {0, 0};
+      if (KVT == PA_KV_FP8_E4M3 && quad) {
+        const int tb = sub * 64;
+        int pos0[4] = {0, 0, 0, 0};
         if (masked) {
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
+          for (int hf = 0; hf < 4; ++hf) {
             const int tk = tb + 16 * hf;
             const int pp = meta->page_pos[tk >> p.ps_shift];
             pos0[hf] = pp < 0 ? -1 : pp + (tk & (p.ps - 1)) + 2 * t;
           }
         }
-        if (KVT == PA_KV_FP8_E4M3)
-          chunk_fp8<SM>(p, st, tb, masked, pos0, cut, g, t, f);
-        else
-          chunk_bf16(p, st, tb, masked, pos0, cut, g, t, lane, f);
+        chunk_fp8<SM, 2>(p, st, tb, masked, pos0, cut, L, g, t, f);
+      } else {
+        for (int tb = sub * tps; tb < (sub + 1) * tps; tb += 32) {
+          int pos0[2] = {0, 0};
+          if (masked) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int tk = tb + 16 * hf;
+              const int pp = meta->page_pos[tk >> p.ps_shift];
+              pos0[hf] = pp < 0 ? -1 : pp + (tk & (p.ps - 1)) + 2 * t;
+            }
+          }
+          if (KVT == PA_KV_FP8_E4M3)
+            chunk_fp8<SM, 1>(p, st, tb, masked, pos0, cut, L, g, t, f);
+          else
+            chunk_bf16(p, st, tb, masked, pos0, cut, meta->page_pos, L, zero_line(sm), g, t, lane, f);
+        }
       }
     }
     __syncwarp();
@@ -248,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     sm.misc()[M_LAST] = 0;
     sm.misc()[M_LAST + 1] = 0;
     sm.misc()[M_WCNT] = 0;
+    for (int k = 0; k < 4; ++k) sm.misc()[M_ZERO + k] = 0;
     fence_barrier_init();
   }
   pdl_launch_dependents();

@@ -46,6 +46,7 @@ static_assert(kNCW * 32 * kConsRegs + 4 * 32 * kProdRegs == kThreads * kLaunchRe
 constexpr int kMaxQ = 8;         // most query tokens per request (m-tiles)
 constexpr int kQRowBytes = kG * kD * 2;   // one query token's 16 heads, bf16
 constexpr int kMergeBytes = 4 * 8192 + 4 * 512;
+constexpr int kUmmaBars = 24;    // extra mbarriers of the tcgen05 kernel
 constexpr int kDumpHeader = 128;
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -270,8 +271,15 @@ struct Smem {
 // M_LAST, M_LAST + 1: merge duty for the head / tail sequence; M_WCNT: writer warps that
 // have stored their part of the head partial; M_WSUM..: 12 warp sums of the prologue scan.
 // M_HEAD, M_TAIL: (request, head, first row, q_len, first CTA, CTA count) of each.
-enum : int { M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24 };
-constexpr int kMiscBytes = 128;
+// M_TMEM: TMEM base address of the tcgen05 kernel.  M_ZERO: a 16-byte line of zeros.
+enum : int {
+  M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24, M_TMEM = 30,
+  M_ZERO = 32
+};
+constexpr int kMiscBytes = 256;
+
+// Shared-window address of the zero line.
+__device__ __forceinline__ uint32_t zero_line(const Smem &sm) { return smem_u32(sm.misc() + M_ZERO); }
 
 __device__ __forceinline__ void raise_flag(const KParams &p, const Smem &sm, uint32_t f) {
   atomicOr(p.status, f);

@@ -23,9 +23,10 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def gpu_run(p, out_dtype="bf16", partition_tokens=0, plan=None, **kw):
+def gpu_run(p, out_dtype="bf16", partition_tokens=0, plan=None, tcgen05=False, **kw):
     d = dv.to_device(p)
-    plan = plan or dv.plan_for(p, out_dtype=out_dtype, partition_tokens=partition_tokens)
+    plan = plan or dv.plan_for(p, out_dtype=out_dtype, partition_tokens=partition_tokens,
+                               tcgen05=tcgen05)
     out, lse = dv.run(plan, p, d, lse=True, **kw)
     torch.cuda.synchronize()
     flags = plan.device_status()
@@ -45,21 +46,48 @@ def check_against_oracle(p, sample=None, what="", **kw):
 
 # ------------------------------------------------------------------------ the workloads
 
-def test_tiny_dense_decode():
-    check_against_oracle(synth.tiny_dense(0), what="tiny dense")
+# FP8 plans with one query token may run the tcgen05 kernel (tcgen05=True) instead of
+# the default mma.sync kernel; both stay covered.
+@pytest.mark.parametrize("tc", [False, True])
+def test_tiny_dense_decode(tc):
+    check_against_oracle(synth.tiny_dense(0), what=f"tiny dense tcgen05={tc}", tcgen05=tc)
 
 
-def test_dense_8k_full_size_sampled():
-    check_against_oracle(synth.dense_8k(1), sample=[0, 13, 31], what="dense 8K")
+@pytest.mark.parametrize("tc", [False, True])
+def test_dense_8k_full_size_sampled(tc):
+    check_against_oracle(synth.dense_8k(1), sample=[0, 13, 31], what=f"dense 8K tcgen05={tc}",
+                         tcgen05=tc)
 
 
 def test_dense_8k_bf16_control():
     check_against_oracle(synth.dense_8k(1, kv_dtype="bf16"), sample=[0, 31], what="bf16 control")
 
 
-@pytest.mark.parametrize("mode", ["scalar", "per_token"])
-def test_long_128k_full_size_sampled(mode):
-    check_against_oracle(synth.long_128k(2, scale_mode=mode), sample=[5], what=f"128K {mode}")
+@pytest.mark.parametrize("mode,tc", [("scalar", False), ("per_token", False), ("scalar", True),
+                                     ("per_token", True)])
+def test_long_128k_full_size_sampled(mode, tc):
+    check_against_oracle(synth.long_128k(2, scale_mode=mode), sample=[5],
+                         what=f"128K {mode} tcgen05={tc}", tcgen05=tc)
+
+
+@pytest.mark.parametrize("kv_dtype,tc,q_len", [("fp8", False, 1), ("fp8", True, 1),
+                                               ("fp8", False, 2), ("bf16", False, 1)])
+def test_nan_codes_in_unattended_slots_stay_unread(kv_dtype, tc, q_len):
+    """Slots past the context length in a request's last page hold NaN codes (bytes a
+    cache may leave behind); they are masked, so the output must equal the oracle's,
+    which never reads them."""
+    p = synth.make_problem(11, num_seqs=3, context_lens=[200, 77, 130], q_lens=[q_len] * 3,
+                           page_size=64, kv_dtype=kv_dtype)
+    nan = 0x7F if kv_dtype == "fp8" else 0x7FC0
+    for r in range(p.num_seqs):
+        L = int(p.context_lens[r])
+        last = int(p.block_table[r, (L - 1) // p.page_size])
+        for o in range(L % p.page_size or p.page_size, p.page_size):
+            p.v_cache[last, :, o, :] = nan
+            p.k_cache[last, :, o, :] = nan
+    out, _ = check_against_oracle(p, what=f"NaN slots {kv_dtype} tcgen05={tc} q_len={q_len}",
+                                  tcgen05=tc)
+    assert np.isfinite(out).all()
 
 
 @pytest.mark.parametrize("batch", ["A", "B"])
