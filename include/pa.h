@@ -74,7 +74,8 @@ enum { PA_OUT_BF16 = 0, PA_OUT_F32 = 1 };
  *   in the stream is finishing, and read the index inputs (block_table, context_lens,
  *   cu_seqlens_q, selected_pages, num_selected) before that kernel has completed; they
  *   wait for it to complete before reading q, the caches or the scales, and before
- *   writing anything.  So with PDL on, the kernel enqueued immediately before pa_decode
+ *   writing anything (before the wait they only ask L2 to prefetch the first pages,
+ *   which reads nothing into the kernel).  So with PDL on, the kernel enqueued immediately before pa_decode
  *   must not write those index inputs (copies and host writes are unaffected).  Set
  *   this flag if it does. */
 #define PA_PLAN_NO_PDL 0x1

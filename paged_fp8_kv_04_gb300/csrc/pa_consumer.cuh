@@ -463,10 +463,12 @@ __device__ __forceinline__ void store_unit(const KParams &p, int tok, int head0,
 // The last CTA to finish a split sequence merges every partial (log-sum-exp merge).
 // Lane-thread u handles fragment units u and u + 256 of an m-tile, which belong to the
 // same two rows, so one batch of independent loads brings the maxima, sums and
-// accumulators of up to 8 partials: one memory round trip per 8 partials.
+// accumulators of up to kMergeBatch partials (12 FP8, 8 BF16, which has less register
+// room): one memory round trip per batch.
 template <int KVT>
 __device__ void merge_partials(const KParams &p, int h, int row0, int qlen, int c_first, int n,
                                int ctid) {
+  constexpr int kMergeBatch = KVT == PA_KV_FP8_E4M3 ? 12 : 8;
   const int units = qlen * kG * 32;
   const float4 *src = reinterpret_cast<const float4 *>(p.part_o);
   const int64_t slot_f4 = (int64_t)(p.mmax / kG) * 512;  // float4s per partial slot
@@ -476,11 +478,11 @@ __device__ void merge_partials(const KParams &p, int h, int row0, int qlen, int 
     const int r0w = mt * kG + gg;
     float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
     float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-    for (int k0 = 0; k0 < n; k0 += 8) {
-      float m0[8], m1[8], l0[8], l1[8];
-      float4 v0[8], v1[8];
+    for (int k0 = 0; k0 < n; k0 += kMergeBatch) {
+      float m0[kMergeBatch], m1[kMergeBatch], l0[kMergeBatch], l1[kMergeBatch];
+      float4 v0[kMergeBatch], v1[kMergeBatch];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kMergeBatch; ++j) {
         if (k0 + j < n) {
           const int64_t sl = slot_of(c_first + k0 + j, c_first);
           const float4 ml = __ldcg(reinterpret_cast<const float4 *>(p.part_ml) +
@@ -499,7 +501,7 @@ __device__ void merge_partials(const KParams &p, int h, int row0, int qlen, int 
       }
       float n0 = M0, n1 = M1;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kMergeBatch; ++j) {
         n0 = fmaxf(n0, m0[j]);
         n1 = fmaxf(n1, m1[j]);
       }
@@ -510,7 +512,7 @@ __device__ void merge_partials(const KParams &p, int h, int row0, int qlen, int 
       L0 *= c0;
       L1 *= c1;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < kMergeBatch; ++j) {
         const float w0 = n0 == -INFINITY ? 0.f : fast_exp2(m0[j] - n0);
         const float w1 = n1 == -INFINITY ? 0.f : fast_exp2(m1[j] - n1);
         a0.x += w0 * v0[j].x; a0.y += w0 * v0[j].y; a0.z += w1 * v0[j].z; a0.w += w1 * v0[j].w;

@@ -82,22 +82,70 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
                                                   : (kDumpHeader + 4 * kTile * kD);
   const int n = b - a;
   bool has_head = false, has_tail = false;  // split sequences (records in misc[])
+  if constexpr (DUMP) {
+    // Gather test hook: every warp visits every tile.
+    for (int i = 0; i < n; ++i) {
+      const int s = i % p.nstage;
+      if (!wait_tile(sm, s, (i / p.nstage) & 1, a + i)) {
+        if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
+        break;
+      }
+      const StageMeta *meta = sm.meta(s);
+      if (meta->flags & F_BEGIN) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.qempty(meta->qslot));
+      }
+      dump_stage<KVT, SM>(p, sm, s, ctid, tile_bytes);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty(s));
+    }
+    return;
+  }
+
+  // The CTA's tiles in order: (request r, KV head h, tile tj of nt), walked locally so
+  // that a warp needs a stage only for the tiles it owns and for each request's first
+  // tile (whose query every warp loads).  Stage arrivals: 1 per warp on a request's
+  // first tile; otherwise the owners alone, weighted so that they count 8.
+  int rw, hw, tjw;
+  locate(tstart, p.num_seqs, p.Hkv, a, rw, hw, tjw);
+  int ntw = tstart[rw + 1] - tstart[rw];
+  int seg = 0, qlen = 1, row0 = 0, L = 0, mode = 0;  // mode 0: quad, 1: paired, 2: all
   for (int i = 0; i < n; ++i) {
     const int s = i % p.nstage;
-    if (!mbar_wait_bounded(sm.full(s), (i / p.nstage) & 1)) {
-      if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
-      break;
+    const int r = rw, h = hw, tj = tjw, nt = ntw, gt = a + i;
+    if (++tjw == ntw) {
+      tjw = 0;
+      if (++hw == p.Hkv) {
+        hw = 0;
+        do {
+          ++rw;
+        } while (rw < p.num_seqs && tstart[rw + 1] == tstart[rw]);
+      }
+      if (rw < p.num_seqs) ntw = tstart[rw + 1] - tstart[rw];
     }
-    const StageMeta *meta = sm.meta(s);
-    const int flags = meta->flags, r = meta->r, h = meta->h;
-    const int qlen = meta->qlen, row0 = meta->row0, L = meta->L;
-    if (flags & F_BEGIN) {
+    const bool begin = (i == 0) || (tj == 0);
+    const bool end = (i == n - 1) || (tj == nt - 1);
+    const bool whole = gt - tj >= a && gt - tj + nt <= b;
+    bool have = false;
+    if (begin) {
+      if (!wait_tile(sm, s, (i / p.nstage) & 1, gt)) {
+        if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
+        break;
+      }
+      have = true;
+      const int qs = seg & 1;
+      ++seg;
+      const int32_t *qh = sm.misc() + M_QHDR + 8 * qs;
+      qlen = qh[2];
+      row0 = qh[3];
+      L = qh[4];
       mt = qlen;
       paired = mt <= 4;
       // FP8 with one query token: four groups of two warps take every fourth tile, each
       // warp a 64-token half (two independent chains per step).
       quad = KVT == PA_KV_FP8_E4M3 && mt == 1;
       if (quad) {
+        mode = 0;
         ts = 2;
         active = true;
         mtile = 0;
@@ -105,6 +153,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
         slice = warp;  // (group, half) = (warp >> 1, warp & 1)
         nsl = 8;
       } else if (paired) {
+        mode = 1;
         const int wl = warp & 3;
         ts = 4 / mt;
         active = wl < mt * ts;
@@ -113,6 +162,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
         slice = (warp >> 2) * ts + sub;
         nsl = 2 * ts;
       } else {
+        mode = 2;
         ts = 1;
         active = warp < mt;
         mtile = warp % mt;
@@ -120,18 +170,23 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
         nsl = 1;
       }
       cut = L - qlen + mtile + 1;
-      if (!DUMP && active) {
-        load_q<KVT>(p, sm.qslot(meta->qslot) + mtile * kQRowBytes, g, t, f);
+      if (active) {
+        load_q<KVT>(p, sm.qslot(qs) + mtile * kQRowBytes, g, t, f);
         reset_state(f);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(sm.qempty(meta->qslot));
+      if (lane == 0) mbar_arrive(sm.qempty(qs));
     }
-    const bool mine = active && (quad ? (i & 3) == (warp >> 1) : (!paired || (i & 1) == (warp >> 2)));
-    if (DUMP) {
-      dump_stage<KVT, SM>(p, sm, s, ctid, tile_bytes);
-    } else if (mine) {
-      const bool masked = (flags & F_MASK) != 0;
+    const bool owner = mode == 0 ? (i & 3) == (warp >> 1) : mode == 1 ? (i & 1) == (warp >> 2) : true;
+    if (owner) {
+      if (!have && !wait_tile(sm, s, (i / p.nstage) & 1, gt)) {
+        if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
+        break;
+      }
+    }
+    if (owner && active) {
+      const StageMeta *meta = sm.meta(s);
+      const bool masked = (meta->flags & F_MASK) != 0;
       const int tps = kTile / ts;
       const uint32_t st = sm.stage(s);
       if (KVT == PA_KV_FP8_E4M3 && quad) {
@@ -164,10 +219,12 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sm.empty(s));
+    if (begin || owner) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cnt(sm.empty(s), begin ? 1u : (mode == 0 ? 4u : mode == 1 ? 2u : 1u));
+    }
 
-    if (DUMP || !(flags & F_END)) continue;
+    if (!end) continue;
 
     // ---- end of this CTA's part of sequence (r, h): merge the token slices -----------
     // Pairs of slices while more than 4 remain, then all remaining into slice 0, so the
@@ -189,7 +246,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       }
     }
     const bool writer = active && slice == 0;
-    if (flags & F_WHOLE) {
+    if (whole) {
       if (writer) write_final<KVT>(p, f, row0 + mtile, h * kG, g, t);
       continue;
     }
@@ -198,7 +255,6 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     // arrival at once (the other warps stream on), so that its merge falls to one of
     // the sequence's other CTAs.  The sequence the CTA leaves unfinished is counted
     // after the last tile.
-    const int nt = tstart[r + 1] - tstart[r];
     const int gs = tstart[r] * p.Hkv + h * nt;
     int c_first, nc;
     seq_ctas(p, tstart, r, h, gs, gs + nt, c_first, nc);
@@ -231,7 +287,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     }
   }
 
-  if (DUMP || !(has_head || has_tail)) return;
+  if (!(has_head || has_tail)) return;
   if (has_tail) {
     __threadfence();
     cons_sync(p, sm, cphase);

@@ -272,11 +272,26 @@ struct Smem {
 // have stored their part of the head partial; M_WSUM..: 12 warp sums of the prologue scan.
 // M_HEAD, M_TAIL: (request, head, first row, q_len, first CTA, CTA count) of each.
 // M_TMEM: TMEM base address of the tcgen05 kernel.  M_ZERO: a 16-byte line of zeros.
+// M_QHDR: (request, KV head, q_len, first row, context) of the request whose query sits
+// in query slot k, at M_QHDR + 8 k; written by the producer with the request's first tile.
 enum : int {
   M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24, M_TMEM = 30,
-  M_ZERO = 32
+  M_ZERO = 32, M_QHDR = 40
 };
 constexpr int kMiscBytes = 256;
+
+// Waits for stage s to hold CTA tile gt (fill parity `parity`).  A consumer that skipped
+// the stage's previous tile may find that fill not yet landed, which the parity alone
+// cannot tell from this one: the tile id the producer wrote decides.
+__device__ __forceinline__ bool wait_tile(const Smem &sm, int s, uint32_t parity, int gt) {
+  const volatile int32_t *id = &sm.meta(s)->gtile;
+  if (mbar_try_wait(sm.full(s), parity) && *id == gt) return true;
+  const long long t0 = clock64();
+  while (!(mbar_try_wait(sm.full(s), parity) && *id == gt)) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
 
 // Shared-window address of the zero line.
 __device__ __forceinline__ uint32_t zero_line(const Smem &sm) { return smem_u32(sm.misc() + M_ZERO); }

@@ -67,7 +67,20 @@ __device__ void run_producer(const KParams &p, const Smem &sm, int a, int b, uin
     }
     if (!waited_deps) {
       // Everything above read only index inputs; q, the caches, the scales and the
-      // workspace wait for the kernels this launch depends on.
+      // workspace wait for the kernels this launch depends on.  Before the wait, only
+      // L2 prefetches of the first tiles' pages: they move nothing into this kernel (its
+      // reads come after the wait, and L2 is where every write lands first), but they
+      // let HBM fetch those pages while the previous kernel finishes.
+      if (gt < b && slot < p.nstage && phys >= 0) {
+        const int32_t rowp = (phys * p.Hkv + h) * ps;
+        const uint32_t rb = (KVT == PA_KV_FP8_E4M3 ? 1u : 2u) * kD;
+        prefetch_l2(p.k_cache + (int64_t)rowp * rb, ps * rb);
+        prefetch_l2(p.v_cache + (int64_t)rowp * rb, ps * rb);
+        if (SM == PA_SCALE_PER_TOKEN) {
+          prefetch_l2(p.k_scale + rowp, ps * 4);
+          prefetch_l2(p.v_scale + rowp, ps * 4);
+        }
+      }
       pdl_wait();
       waited_deps = true;
       if (report) atomicOr(p.status, report);
@@ -125,6 +138,14 @@ __device__ void run_producer(const KParams &p, const Smem &sm, int a, int b, uin
         mt->nvalid = __popc(valid_bits & slot_bits);
         mt->gtile = gtj;
         mt->qslot = qs;
+        if (begin) {
+          int32_t *qh = sm.misc() + M_QHDR + 8 * qs;
+          qh[0] = rj;
+          qh[1] = hj;
+          qh[2] = qj;
+          qh[3] = row0j;
+          qh[4] = Lj;
+        }
       }
       __syncwarp();
       const uint32_t tx = __popc(valid_bits & slot_bits) * pbytes +

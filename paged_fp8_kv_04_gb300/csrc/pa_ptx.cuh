@@ -51,6 +51,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
       : "memory");
 }
 
+// Arrival that counts `cnt` times towards the phase.
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t cnt) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(cnt)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
