@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = balanced)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--tcgen05", action="store_true",
+                    help="FP8 plans with one query token: run the tcgen05 kernel (PA_PLAN_TCGEN05)")
     ap.add_argument("--profile", type=int, default=0,
                     help="only run --warmup + this many direct pa_decode calls (for ncu)")
     return ap.parse_args()
@@ -54,8 +56,8 @@ def parse():
 # from one ncu capture per workload, valid only for the kernel sources they were taken on
 # (sha256 over the CUDA sources and the C header); any other source gives traffic null.
 MEASURED_TRAFFIC = {
-    "dense8k": {"bytes": 69424896 + 767744,
-                "csrc_sha256": "9e6b878cb6d7fcbe54fd0619bffa7ef7ef354d735a05ea37b71a816adc1cfeb5",
+    "dense8k": {"bytes": 69448448 + 777728,
+                "csrc_sha256": "224c60eb52007071dda813b84b67ddd10887155101801a6118e1b13a9690d6e6",
                 "profile": "profiles/decode_kernel_dense8k_full.md"},
 }
 
@@ -285,7 +287,7 @@ def bench_ours(args):
 
     p, desc = make_workload(args.workload)
     d = dv.to_device(p, dev)
-    plan = dv.plan_for(p, device=dev, partition_tokens=args.partition)
+    plan = dv.plan_for(p, device=dev, partition_tokens=args.partition, tcgen05=args.tcgen05)
     total_bytes, kv_bytes = algorithmic_bytes(p)
 
     # Rotating copies of the KV cache (and scales) so that no call finds its KV in L2.
@@ -420,6 +422,7 @@ def bench_ours(args):
         if p.kv_dtype == "fp8" else "bf16 mma, f32 accumulate", "data": "synthetic",
         "config": {"workload": desc, "l2": f"{npools} rotating KV copies ({npools * pool_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                    "timed": "CUDA graph replay of back-to-back pa_decode calls",
+                   "kernel": "tcgen05" if args.tcgen05 and plan.info()["kernel"] == 1 else "mma.sync",
                    "grid_ctas": info["grid_ctas"], "stages": info["stages"],
                    "partition_tokens": args.partition},
         "pct_of_peak": 100.0 * achieved / peak,

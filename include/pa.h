@@ -152,6 +152,8 @@ typedef struct pa_plan_info {
   int64_t smem_bytes;         /* dynamic shared memory per CTA */
   int64_t workspace_bytes;
   int64_t partial_slots;      /* split-K partial (m, l, o) slots in the workspace */
+  int32_t kernel;             /* decode kernel of the plan: 0 mma.sync, 1 tcgen05 (PA_PLAN_TCGEN05) */
+  int32_t reserved;
 } pa_plan_info_t;
 
 typedef struct pa_plan pa_plan_t;

@@ -61,7 +61,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("grid_ctas", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("threads_per_cta", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("partial_slots", ctypes.c_int64)]
+                ("partial_slots", ctypes.c_int64), ("kernel", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib = None

@@ -557,6 +557,8 @@ pa_status_t pa_plan_get_info(const pa_plan_t *plan, pa_plan_info_t *info) {
   info->smem_bytes = (int64_t)plan->geo.smem;
   info->workspace_bytes = (int64_t)plan->geo.ws;
   info->partial_slots = plan->geo.slots;
+  info->kernel = use_umma(plan->desc) ? 1 : 0;
+  info->reserved = 0;
   return PA_OK;
 }
 
