@@ -170,22 +170,6 @@ __device__ void run_producer(const KParams &p, const Smem &sm, int a, int b, uin
           tma_load_2d(st + 49152 + po, &p.tm_v, 64, row, fb, pol);
         }
       }
-      // L2 prefetch of the pages of tile j + nstage, whose TMA copy is issued once tile j
-      // is released: the copy then finds its bytes in L2 instead of waiting on HBM.
-      {
-        const int jp = j + p.nstage;
-        const int ph_src = jp * ppt;
-        if (jp < nbat && lane >= ph_src && lane < ph_src + ppt && phys >= 0) {
-          const int32_t rowp = (phys * p.Hkv + h) * ps;
-          const uint32_t rb = (KVT == PA_KV_FP8_E4M3 ? 1u : 2u) * kD;
-          prefetch_l2(p.k_cache + (int64_t)rowp * rb, ps * rb);
-          prefetch_l2(p.v_cache + (int64_t)rowp * rb, ps * rb);
-          if (SM == PA_SCALE_PER_TOKEN) {
-            prefetch_l2(p.k_scale + rowp, ps * 4);
-            prefetch_l2(p.v_scale + rowp, ps * 4);
-          }
-        }
-      }
       if (begin && lane < qj) {
         const uint16_t *qsrc = p.q + ((int64_t)(row0j + lane) * (p.Hkv * kG) + hj * kG) * kD;
         bulk_load(sm.qslot(qs) + lane * kQRowBytes, qsrc, kQRowBytes, fb);
