@@ -128,7 +128,7 @@ pa_status_t geometry(const pa_plan_desc_t *d, Geometry *g) {
     const size_t off_merge = off;
     off += pa::kMergeBytes;
     const size_t off_tstart = off;
-    off += round_up((size_t)(d->max_batch + 1) * 4, 16);
+    off += round_up((size_t)(2 * d->max_batch + 4) * 4, 16);  // tstart, then the CTA prefix
     const size_t off_meta = off;
     off += (size_t)ns * sizeof(pa::StageMeta);
     const size_t off_bar = off;

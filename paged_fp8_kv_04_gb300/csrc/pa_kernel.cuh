@@ -134,17 +134,30 @@ __device__ __forceinline__ ReqInfo request_info(const KParams &p, int r, uint32_
 
 // Exclusive prefix of tile counts over requests into tstart[0..B] (shared memory).
 // Returns this thread's PA_DEV_* flags (reported once the kernel may write).
-__device__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum) {
+//
+// Then the CTA schedule (balanced mode).  When there are no more sequences (request, KV
+// head) than CTAs, every sequence gets a whole number of CTAs: the smallest budget X of
+// work per CTA (tiles x query tokens) with sum_r ceil(nt_r q_r / X) <= floor(grid / Hkv)
+// is found by bisection, and sequence r gets k_r = min(nt_r, ceil(nt_r q_r / X)) CTAs of
+// equal shares.  No CTA then holds the end of one sequence and the start of another, which
+// would stop all of its warps for a merge in mid-stream.  cstart = tstart + B + 2 holds
+// the exclusive prefix of k_r * Hkv, and cstart[B + 1] = 1 marks this mode.  Otherwise
+// CTAs take equal chunks of ceil(T / grid) tiles.
+// (Not inlined: it runs once, and its temporaries must not crowd the loops' registers.)
+__device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kThreads / 32;
   const int B = p.num_seqs;
   const int per = (B + kThreads - 1) / kThreads;
   const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+  int32_t *cst = tstart + B + 2;
   uint32_t fl = 0;
   int local = 0;
   for (int r = r0; r < r1; ++r) {
-    const int n = request_info(p, r, fl).tiles;
-    tstart[r] = n;
-    local += n;
+    const ReqInfo ri = request_info(p, r, fl);
+    tstart[r] = ri.tiles;
+    cst[r] = ri.tiles * max(ri.qlen, 1);  // work of one head of the request (until replaced)
+    local += ri.tiles;
   }
   int inc = local;
 #pragma unroll
@@ -156,7 +169,7 @@ __device__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum)
   __syncthreads();
   if (tid == 0) {
     int run = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const int v = wsum[w];
       wsum[w] = run;
       run += v;
@@ -169,6 +182,68 @@ __device__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum)
     const int n = tstart[r];
     tstart[r] = run;
     run += n;
+  }
+  __syncthreads();
+  if (warp == 0) {  // the schedule: one warp, no further block barriers
+    const uint32_t full = 0xffffffffu;
+    uint32_t ne = 0, wm = 0;
+    unsigned long long wt = 0;
+    for (int r = lane; r < B; r += 32) {
+      const int nt = tstart[r + 1] - tstart[r];
+      ne += nt > 0;
+      wt += (uint32_t)cst[r];
+      wm = max(wm, (uint32_t)cst[r]);
+    }
+    ne = __reduce_add_sync(full, ne);
+    wm = __reduce_max_sync(full, wm);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) wt += __shfl_xor_sync(full, wt, o);
+    const uint32_t G = (uint32_t)(p.grid / p.Hkv);
+    const bool aligned = !p.sched_partition && tstart[B] > 0 && ne <= G;
+    if (aligned) {
+      // lower bound: the average work per CTA; upper bounds that are feasible: the largest
+      // request (one CTA each), and W / (G - E) (sum ceil(w / X) < W / X + E <= G).
+      uint32_t lo = (uint32_t)((wt + G - 1) / G), hi = wm;
+      if (lo < 1) lo = 1;
+      if (G > ne) {
+        const unsigned long long b = (wt + (G - ne) - 1) / (G - ne);
+        if (b < hi) hi = (uint32_t)b;
+      }
+      if (hi < lo) lo = hi;
+      while (lo < hi) {
+        const uint32_t mid = (lo + hi) >> 1;
+        uint32_t cnt = 0;
+        for (int r = lane; r < B; r += 32) {
+          const uint32_t nt = (uint32_t)(tstart[r + 1] - tstart[r]);
+          const uint32_t q = ((uint32_t)cst[r] + mid - 1) / mid;
+          cnt += min(q, nt);
+        }
+        cnt = __reduce_add_sync(full, cnt);
+        if (cnt <= G)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      int carry = 0;
+      for (int c0 = 0; c0 < B; c0 += 32) {
+        const int r = c0 + lane;
+        int k = 0;
+        if (r < B) {
+          const uint32_t nt = (uint32_t)(tstart[r + 1] - tstart[r]);
+          k = (int)min(((uint32_t)cst[r] + lo - 1) / lo, nt) * p.Hkv;
+        }
+        int kin = k;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(full, kin, o);
+          if (lane >= o) kin += v;
+        }
+        if (r < B) cst[r] = carry + kin - k;
+        carry += __shfl_sync(full, kin, 31);
+      }
+      if (lane == 0) cst[B] = carry;
+    }
+    if (lane == 0) cst[B + 1] = aligned ? 1 : 0;
   }
   __syncthreads();
   return fl;
@@ -193,10 +268,29 @@ __device__ __forceinline__ void locate(const int32_t *tstart, int B, int Hkv, in
 }
 
 // The CTA's tile range [a, b).
-__device__ __forceinline__ void cta_range(const KParams &p, const int32_t *tstart, int c, int &a,
-                                          int &b) {
-  const int T = tstart[p.num_seqs] * p.Hkv;
+__device__ __noinline__ void cta_range(const KParams &p, const int32_t *tstart, int c, int &a,
+                                       int &b) {
+  const int B = p.num_seqs, T = tstart[B] * p.Hkv;
   if (!p.sched_partition) {
+    const int32_t *cst = tstart + B + 2;
+    if (cst[B + 1]) {  // sequence-aligned: chunk j of the k CTAs of sequence (r, h)
+      a = b = T;
+      if (c >= cst[B]) return;
+      int lo = 0, hi = B - 1;  // first r with cst[r + 1] > c
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cst[mid + 1] > c)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      const int r = lo, k = (cst[r + 1] - cst[r]) / p.Hkv, loc = c - cst[r];
+      const int h = loc / k, j = loc - h * k, nt = tstart[r + 1] - tstart[r];
+      const int gs = tstart[r] * p.Hkv + h * nt;
+      a = gs + (int)((int64_t)j * nt / k);
+      b = gs + (int)((int64_t)(j + 1) * nt / k);
+      return;
+    }
     const int C = (T + p.grid - 1) / p.grid;
     a = min(T, c * C);
     b = min(T, a + C);
@@ -205,7 +299,7 @@ __device__ __forceinline__ void cta_range(const KParams &p, const int32_t *tstar
   const int s = c / p.maxch, k = c - s * p.maxch;
   const int r = s / p.Hkv, h = s - r * p.Hkv;
   a = b = 0;
-  if (r >= p.num_seqs) return;
+  if (r >= B) return;
   const int nt = tstart[r + 1] - tstart[r];
   const int gs = tstart[r] * p.Hkv + h * nt, ge = gs + nt;
   a = min(ge, gs + k * p.part_tiles);
@@ -216,6 +310,13 @@ __device__ __forceinline__ void cta_range(const KParams &p, const int32_t *tstar
 __device__ __forceinline__ void seq_ctas(const KParams &p, const int32_t *tstart, int r, int h,
                                          int gs, int ge, int &c_first, int &n) {
   if (!p.sched_partition) {
+    const int32_t *cst = tstart + p.num_seqs + 2;
+    if (cst[p.num_seqs + 1]) {
+      const int k = (cst[r + 1] - cst[r]) / p.Hkv;
+      c_first = cst[r] + h * k;
+      n = k;
+      return;
+    }
     const int T = tstart[p.num_seqs] * p.Hkv;
     const int C = (T + p.grid - 1) / p.grid;
     c_first = gs / C;
