@@ -334,11 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   pdl_launch_dependents();
   const uint32_t fl = scan_tiles(p, sm.tstart(), sm.misc() + M_WSUM);
   const uint32_t report = blockIdx.x == 0 ? fl : 0u;
-  int a, b;
-  cta_range(p, sm.tstart(), blockIdx.x, a, b);
   if (warp >= kNCW) {
     regs_dec<kProdRegs>();
     if (warp != kNCW) return;  // the rest of the producer warpgroup only gives registers
+    const int a = sm.misc()[M_WSUM], b = sm.misc()[M_WSUM + 1];
     // The producer reads index inputs before the wait, q and the caches after it.
     if (a < b) run_producer<KVT, SM>(p, sm, a, b, report);
     else {
@@ -348,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     return;
   }
   regs_inc<kConsRegs>();
+  const int a = sm.misc()[M_WSUM], b = sm.misc()[M_WSUM + 1];
   pdl_wait();  // consumers write outputs and the workspace
   if (report) atomicOr(p.status, report);
   run_consumer<KVT, SM, DUMP>(p, sm, a, b, warp, lane);

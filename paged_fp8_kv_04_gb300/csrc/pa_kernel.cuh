@@ -132,17 +132,67 @@ __device__ __forceinline__ ReqInfo request_info(const KParams &p, int r, uint32_
   return ri;
 }
 
+// The CTA's tile range [a, b).
+__device__ __forceinline__ void cta_range(const KParams &p, const int32_t *tstart, int c, int &a,
+                                       int &b) {
+  const int B = p.num_seqs, T = tstart[B] * p.Hkv;
+  if (!p.sched_partition) {
+    const int32_t *cst = tstart + B + 2;
+    if (cst[B + 1]) {  // sequence-aligned: chunk j of the k CTAs of sequence (r, h)
+      a = b = T;
+      if (c >= cst[B]) return;
+      int lo = 0, hi = B - 1;  // first r with cst[r + 1] > c
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cst[mid + 1] > c)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      const int r = lo, k = (cst[r + 1] - cst[r]) / p.Hkv, loc = c - cst[r];
+      const int h = loc / k, j = loc - h * k, nt = tstart[r + 1] - tstart[r];
+      const int gs = tstart[r] * p.Hkv + h * nt;
+      const int s_last = cst[B + 1] >> 1;
+      if (s_last > 0 && h == p.Hkv - 1 && cst[r + 1] == cst[B]) {
+        // the grid's last sequence: its last CTA takes s_last tiles, the others share the rest
+        const int rest = nt - s_last;
+        a = gs + (j < k - 1 ? j * rest / (k - 1) : rest);
+        b = gs + (j < k - 1 ? (j + 1) * rest / (k - 1) : nt);
+        return;
+      }
+      a = gs + j * nt / k;
+      b = gs + (j + 1) * nt / k;
+      return;
+    }
+    const int C = (T + p.grid - 1) / p.grid;
+    a = min(T, c * C);
+    b = min(T, a + C);
+    return;
+  }
+  const int s = c / p.maxch, k = c - s * p.maxch;
+  const int r = s / p.Hkv, h = s - r * p.Hkv;
+  a = b = 0;
+  if (r >= B) return;
+  const int nt = tstart[r + 1] - tstart[r];
+  const int gs = tstart[r] * p.Hkv + h * nt, ge = gs + nt;
+  a = min(ge, gs + k * p.part_tiles);
+  b = min(ge, a + p.part_tiles);
+}
+
 // Exclusive prefix of tile counts over requests into tstart[0..B] (shared memory).
-// Returns this thread's PA_DEV_* flags (reported once the kernel may write).
+// Returns this thread's PA_DEV_* flags (reported once the kernel may write) and leaves
+// the CTA's tile range [a, b) in wsum[0], wsum[1].
 //
 // Then the CTA schedule (balanced mode).  When there are no more sequences (request, KV
-// head) than CTAs, every sequence gets a whole number of CTAs: the smallest budget X of
+// head) than CTAs, every sequence may get a whole number of CTAs: the smallest budget X of
 // work per CTA (tiles x query tokens) with sum_r ceil(nt_r q_r / X) <= floor(grid / Hkv)
 // is found by bisection, and sequence r gets k_r = min(nt_r, ceil(nt_r q_r / X)) CTAs of
 // equal shares.  No CTA then holds the end of one sequence and the start of another, which
-// would stop all of its warps for a merge in mid-stream.  cstart = tstart + B + 2 holds
-// the exclusive prefix of k_r * Hkv, and cstart[B + 1] = 1 marks this mode.  Otherwise
-// CTAs take equal chunks of ceil(T / grid) tiles.
+// would stop all of its warps for a merge in mid-stream.  This is taken when X is no
+// larger than (C + 2) q_max, C = ceil(T / grid) tiles being the equal chunk of the other
+// mode.  cstart = tstart + B + 2 holds the exclusive prefix of k_r * Hkv; cstart[B + 1] =
+// 1 + 2 s marks this mode, s > 0 being the share of the grid's last CTA when no CTA is
+// left over.  Otherwise (cstart[B + 1] = 0) CTAs take equal chunks of C tiles.
 // (Not inlined: it runs once, and its temporaries must not crowd the loops' registers.)
 __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, int32_t *wsum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -186,24 +236,28 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
   __syncthreads();
   if (warp == 0) {  // the schedule: one warp, no further block barriers
     const uint32_t full = 0xffffffffu;
-    uint32_t ne = 0, wm = 0;
+    uint32_t ne = 0, wm = 0, qm = 1;
     unsigned long long wt = 0;
     for (int r = lane; r < B; r += 32) {
       const int nt = tstart[r + 1] - tstart[r];
       ne += nt > 0;
       wt += (uint32_t)cst[r];
       wm = max(wm, (uint32_t)cst[r]);
+      if (nt > 0) qm = max(qm, (uint32_t)(cst[r] / nt));
     }
     ne = __reduce_add_sync(full, ne);
     wm = __reduce_max_sync(full, wm);
+    qm = __reduce_max_sync(full, qm);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) wt += __shfl_xor_sync(full, wt, o);
     const uint32_t G = (uint32_t)(p.grid / p.Hkv);
-    const bool aligned = !p.sched_partition && tstart[B] > 0 && ne <= G;
+    bool aligned = !p.sched_partition && tstart[B] > 0 && ne <= G;
+    uint32_t lo = 1;
     if (aligned) {
       // lower bound: the average work per CTA; upper bounds that are feasible: the largest
       // request (one CTA each), and W / (G - E) (sum ceil(w / X) < W / X + E <= G).
-      uint32_t lo = (uint32_t)((wt + G - 1) / G), hi = wm;
+      lo = (uint32_t)((wt + G - 1) / G);
+      uint32_t hi = wm;
       if (lo < 1) lo = 1;
       if (G > ne) {
         const unsigned long long b = (wt + (G - ne) - 1) / (G - ne);
@@ -224,14 +278,51 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
         else
           lo = mid + 1;
       }
+      // Against equal chunks of C = ceil(T / grid) tiles, whose CTAs may straddle two
+      // sequences (a merge in mid-stream, some two tile-times): whole sequences only while
+      // their budget is no larger than such a chunk's worst case.
+      const uint32_t T = (uint32_t)tstart[B] * (uint32_t)p.Hkv;
+      const uint32_t C = (T + (uint32_t)p.grid - 1) / (uint32_t)p.grid;
+      aligned = lo <= (C + 2) * qm;
+    }
+    if (aligned) {
+      // k_r at that budget (cst[r] turns from work into k_r, lane by lane), and the last
+      // request that has CTAs.
+      uint32_t tot = 0;
+      int r_last = -1, q_last = 1;
+      for (int c0 = 0; c0 < B; c0 += 32) {
+        const int r = c0 + lane;
+        int k = 0, nt = 0, w = 0;
+        if (r < B) {
+          nt = tstart[r + 1] - tstart[r];
+          w = cst[r];
+          k = (int)min(((uint32_t)w + lo - 1) / lo, (uint32_t)nt);
+          cst[r] = k;
+        }
+        tot += (uint32_t)k;
+        const unsigned used = __ballot_sync(full, k > 0);
+        if (used) {
+          const int top = 31 - __clz(used);
+          q_last = __shfl_sync(full, nt > 0 ? w / nt : 1, top);
+          r_last = c0 + top;
+        }
+      }
+      tot = __reduce_add_sync(full, tot);
+      __syncwarp();
+      // With no CTA left over, the last CTA of the grid starts last (after the previous
+      // launch's final merge and its own prologue, some 6 tile-times at one query token):
+      // it takes fewer tiles.  (CTAs left over sit at the end of the grid and take those
+      // late SMs themselves.)
+      int s_last = 0;
+      if (tot == G && r_last >= 0) {
+        const int nt = tstart[r_last + 1] - tstart[r_last], k = cst[r_last];
+        const int q = max(q_last, 1), pt = max(1, (6 + q / 2) / q);
+        if (k >= 2) s_last = max(1, nt / k - pt);
+      }
       int carry = 0;
       for (int c0 = 0; c0 < B; c0 += 32) {
         const int r = c0 + lane;
-        int k = 0;
-        if (r < B) {
-          const uint32_t nt = (uint32_t)(tstart[r + 1] - tstart[r]);
-          k = (int)min(((uint32_t)cst[r] + lo - 1) / lo, nt) * p.Hkv;
-        }
+        const int k = r < B ? cst[r] * p.Hkv : 0;
         int kin = k;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -241,9 +332,20 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
         if (r < B) cst[r] = carry + kin - k;
         carry += __shfl_sync(full, kin, 31);
       }
-      if (lane == 0) cst[B] = carry;
+      if (lane == 0) {
+        cst[B] = carry;
+        cst[B + 1] = 1 + 2 * s_last;
+      }
+    } else if (lane == 0) {
+      cst[B + 1] = 0;
     }
-    if (lane == 0) cst[B + 1] = aligned ? 1 : 0;
+    __syncwarp();
+    if (lane == 0) {  // this CTA's range, for every thread (wsum is free by now)
+      int a, b;
+      cta_range(p, tstart, blockIdx.x, a, b);
+      wsum[0] = a;
+      wsum[1] = b;
+    }
   }
   __syncthreads();
   return fl;
@@ -265,45 +367,6 @@ __device__ __forceinline__ void locate(const int32_t *tstart, int B, int Hkv, in
   const int off = gt - tstart[r] * Hkv;
   h = off / nt;
   tile = off - h * nt;
-}
-
-// The CTA's tile range [a, b).
-__device__ __noinline__ void cta_range(const KParams &p, const int32_t *tstart, int c, int &a,
-                                       int &b) {
-  const int B = p.num_seqs, T = tstart[B] * p.Hkv;
-  if (!p.sched_partition) {
-    const int32_t *cst = tstart + B + 2;
-    if (cst[B + 1]) {  // sequence-aligned: chunk j of the k CTAs of sequence (r, h)
-      a = b = T;
-      if (c >= cst[B]) return;
-      int lo = 0, hi = B - 1;  // first r with cst[r + 1] > c
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (cst[mid + 1] > c)
-          hi = mid;
-        else
-          lo = mid + 1;
-      }
-      const int r = lo, k = (cst[r + 1] - cst[r]) / p.Hkv, loc = c - cst[r];
-      const int h = loc / k, j = loc - h * k, nt = tstart[r + 1] - tstart[r];
-      const int gs = tstart[r] * p.Hkv + h * nt;
-      a = gs + (int)((int64_t)j * nt / k);
-      b = gs + (int)((int64_t)(j + 1) * nt / k);
-      return;
-    }
-    const int C = (T + p.grid - 1) / p.grid;
-    a = min(T, c * C);
-    b = min(T, a + C);
-    return;
-  }
-  const int s = c / p.maxch, k = c - s * p.maxch;
-  const int r = s / p.Hkv, h = s - r * p.Hkv;
-  a = b = 0;
-  if (r >= B) return;
-  const int nt = tstart[r + 1] - tstart[r];
-  const int gs = tstart[r] * p.Hkv + h * nt, ge = gs + nt;
-  a = min(ge, gs + k * p.part_tiles);
-  b = min(ge, a + p.part_tiles);
 }
 
 // CTAs that hold partials of sequence (r, h) whose tiles are [gs, ge).

@@ -632,10 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_umma_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tm = (uint32_t)sm.misc()[M_TMEM];
   const uint32_t report = blockIdx.x == 0 ? fl : 0u;
-  int a, b;
-  cta_range(p, sm.tstart(), blockIdx.x, a, b);
   if (warp >= kNCW) {
     regs_dec<kProdRegs>();
+    const int a = sm.misc()[M_WSUM], b = sm.misc()[M_WSUM + 1];
     if (warp == kNCW) {
       // The producer reads index inputs before the wait, q and the caches after it.
       if (a < b) run_producer<PA_KV_FP8_E4M3, SM>(p, sm, a, b, report);
@@ -656,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_umma_kernel(const __grid_c
     return;
   }
   regs_inc<kConsRegs>();
+  const int a = sm.misc()[M_WSUM], b = sm.misc()[M_WSUM + 1];
   pdl_wait();  // softmax warps write outputs and the workspace
   if (report) atomicOr(p.status, report);
   run_softmax<SM>(p, sm, ub, a, b, tm, warp, lane);
