@@ -16,6 +16,7 @@ is the sum over ranks divided by the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -41,7 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dense8k",
                     choices=["dense8k", "bf16ctl", "long128k_scalar", "long128k", "ragged",
-                             "sparse"])
+                             "sparse", "kv_write"])
     ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = balanced)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -217,11 +218,39 @@ def time_oracle(p, target_s=10.0):
     return total * passes / dt / 1e9, p.num_rows * passes / dt, dt, cores, passes
 
 
+def bench_reference_kv_write(args):
+    from oracle import oracle as O
+    from paged_fp8_kv_04_gb300 import synth
+    c = synth.kv_write_prefill_8k(5)
+    n = 16384
+    sub = dataclasses.replace(c, k_new=c.k_new[:n], v_new=c.v_new[:n], slot_mapping=c.slot_mapping[:n])
+    bufs = (c.k_cache.copy(), c.v_cache.copy(), c.k_scale.copy(), c.v_scale.copy())
+    for _ in range(args.warmup):
+        O.kv_quantize_write(sub.k_new, sub.v_new, sub.slot_mapping, *bufs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.kv_quantize_write(sub.k_new, sub.v_new, sub.slot_mapping, *bufs)
+    dt = time.perf_counter() - t0
+    value = kv_write_bytes(sub) * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": KV_WRITE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 decisions, exact e4m3 rounding", "data": "synthetic",
+        "config": {"workload": c.name, "sample": f"the first {n} tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"the first {n} tokens of the workload"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def bench_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
-    import dataclasses
+    if args.workload == "kv_write":
+        return bench_reference_kv_write(args)
     p, desc = make_workload(args.workload)
     cores = os.cpu_count() or 1
     # Each step: `cores` requests of the workload, each truncated to n leading tokens, so
@@ -285,6 +314,8 @@ def bench_ours(args):
         __graft_entry__.build()
     from paged_fp8_kv_04_gb300 import device as dv
 
+    if args.workload == "kv_write":
+        return bench_kv_write(args, dev, rank, world, local)
     p, desc = make_workload(args.workload)
     d = dv.to_device(p, dev)
     plan = dv.plan_for(p, device=dev, partition_tokens=args.partition, tcgen05=args.tcgen05)
@@ -434,6 +465,121 @@ def bench_ours(args):
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clk,
         "device_flags": flags,
+    }
+    print(json.dumps(line), flush=True)
+
+
+KV_WRITE_METRIC = "FP8 KV quantise-and-write: achieved HBM GB/s (% of GB300 peak)"
+
+
+def kv_write_bytes(c):
+    """bf16 K and V in, e4m3 codes and fp32 scales out, one int64 slot per token."""
+    T, Hkv, D = c.k_new.shape
+    live = int((c.slot_mapping >= 0).sum())
+    return live * Hkv * (2 * 2 * D + 2 * (D + 4)) + T * 8
+
+
+def bench_kv_write(args, dev, rank, world, local):
+    """pa_kv_quantize_write over the dense-8K batch written at once (262144 tokens)."""
+    import torch
+    from paged_fp8_kv_04_gb300 import binding as B, synth
+    c = synth.kv_write_prefill_8k(5)
+    desc = c.name
+    to = lambda a: (torch.from_numpy(a).view(torch.int16) if a.dtype == np.uint16
+                    else torch.from_numpy(a)).to(dev)
+    k0, v0 = to(c.k_new), to(c.v_new)
+    ins = [(k0, v0), (k0.clone(), v0.clone())]   # two 134-MB input sets alternate (> L2)
+    slots = to(c.slot_mapping)
+    kc, vc, ks, vs = to(c.k_cache), to(c.v_cache), to(c.k_scale), to(c.v_scale)
+    total_bytes = kv_write_bytes(c)
+    alist = [B.kv_write_args(k, v, slots, kc, vc, ks, vs) for k, v in ins]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            B.kv_quantize_write(None, None, None, kc, None, None, None, stream=stream,
+                                args=alist[i % 2])
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    chunk = max(c_ for c_ in range(1, min(K, 200) + 1) if K % c_ == 0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            B.kv_quantize_write(None, None, None, kc, None, None, None, stream=stream,
+                                args=alist[i % 2])
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K // chunk):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    us = ms / K * 1e3
+    achieved = total_bytes / (us * 1e-6) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        hk, hv, hs = (x.cpu().pin_memory() for x in (k0, v0, slots))
+        hkc = torch.empty(kc.shape, dtype=kc.dtype).pin_memory()
+        hks = torch.empty(ks.shape, dtype=ks.dtype).pin_memory()
+        dk, dv_, ds = torch.empty_like(k0), torch.empty_like(v0), torch.empty_like(slots)
+        a = B.kv_write_args(dk, dv_, ds, kc, vc, ks, vs)
+        steps = 10
+        with torch.cuda.stream(stream):
+            for it in range(steps + 2):
+                if it == 2:
+                    torch.cuda.synchronize(dev)
+                    t0 = time.perf_counter()
+                dk.copy_(hk, non_blocking=True)
+                dv_.copy_(hv, non_blocking=True)
+                ds.copy_(hs, non_blocking=True)
+                B.kv_quantize_write(None, None, None, kc, None, None, None, stream=stream, args=a)
+                hkc.copy_(kc, non_blocking=True)
+                hks.copy_(ks, non_blocking=True)
+            torch.cuda.synchronize(dev)
+        dt = (time.perf_counter() - t0) / steps
+        e2e = {"value": total_bytes / dt / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(sum(x.numel() * x.element_size() for x in (hk, hv, hs))),
+               "d2h_bytes_per_step": int(hkc.numel() + hks.numel() * 4),
+               "ms_per_step": dt * 1e3,
+               "note": "K codes and K scales read back; V stays on the device"}
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu:
+        from oracle import oracle as O
+        n = 16384
+        sub = dataclasses.replace(c, k_new=c.k_new[:n], v_new=c.v_new[:n],
+                                  slot_mapping=c.slot_mapping[:n])
+        kcc, vcc, kss, vss = c.k_cache.copy(), c.v_cache.copy(), c.k_scale.copy(), c.v_scale.copy()
+        t0 = time.perf_counter()
+        passes = 0
+        while time.perf_counter() - t0 < 5.0:
+            O.kv_quantize_write(sub.k_new, sub.v_new, sub.slot_mapping, kcc, vcc, kss, vss)
+            passes += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": kv_write_bytes(sub) * passes / dt / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"the first {n} tokens, {passes} times, {dt:.1f} s"}
+    peak, peak_kind = peak_hbm()
+    line = {
+        "metric": KV_WRITE_METRIC, "value": achieved, "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 scale, e4m3 out",
+        "data": "synthetic",
+        "config": {"workload": desc, "l2": "two 134 MB input sets alternate (> L2)",
+                   "timed": "CUDA graph replay of back-to-back pa_kv_quantize_write calls"},
+        "us_per_call_graph": us, "algorithmic_bytes_per_call": int(total_bytes),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
 

@@ -67,6 +67,7 @@ enum { PA_OUT_BF16 = 0, PA_OUT_F32 = 1 };
 #define PA_DEV_Q_RANGE       0x20u  /* a query value outside the f16 range (|q| > 65504) */
 #define PA_DEV_TIMEOUT       0x40u  /* a bounded wait inside a kernel gave up (the output is incomplete) */
 #define PA_DEV_DUMP_RANGE    0x80u  /* pa_debug_gather's buffer was too small for the schedule */
+#define PA_DEV_BAD_SLOT      0x100u /* pa_kv_quantize_write: a slot >= num_pages * page_size */
 
 /* Plan flags.
  * PA_PLAN_NO_PDL: launch pa_decode as an ordinary kernel.  By default it is launched
@@ -225,6 +226,47 @@ const char *pa_status_string(pa_status_t status);
  *  - Device-side data flags (PA_DEV_*) of these calls are not reported. */
 pa_status_t pa_decode_noalloc(const pa_plan_desc_t *desc, const pa_decode_args_t *args,
                               void *stream);
+
+/* ---- the producer of the cache: per-token FP8 quantise-and-write ---- */
+
+/* Arguments of pa_kv_quantize_write.  All pointers are device pointers. */
+typedef struct pa_kv_write_args {
+  const void *k_new;             /* bf16 [num_tokens, num_kv_heads, head_dim], 16-B aligned */
+  const void *v_new;             /* bf16, same shape */
+  const int64_t *slot_mapping;   /* [num_tokens]: cache slot page * page_size + offset of each
+                                    token; a negative slot skips the token */
+  void *k_cache;                 /* e4m3 bytes [num_pages, num_kv_heads, page_size, head_dim], 16-B aligned */
+  void *v_cache;
+  float *k_scale;                /* fp32 [num_pages, num_kv_heads, page_size], 4-B aligned */
+  float *v_scale;
+  uint32_t *status;              /* nullable; PA_DEV_BAD_SLOT is OR-ed in when a slot is past the cache */
+  int64_t num_tokens;            /* >= 0; 0 enqueues nothing */
+  int64_t num_pages;
+  int32_t num_kv_heads;          /* >= 1 */
+  int32_t head_dim;              /* 128 */
+  int32_t page_size;             /* 16, 32, 64 or 128 */
+  int32_t reserved;              /* 0 */
+} pa_kv_write_args_t;
+
+/* Quantises new K and V rows to the per-token FP8 cache that pa_decode reads (ROCm/ATOM
+ * PR 2614: MiniMax-M3 writes FP8 KV plus per-token K/V scales, checked by a
+ * producer-to-consumer operator test; ROCm/ATOM PR 2710, "Smaller": the cache-write
+ * branch).  For every token t with slot s = slot_mapping[t] >= 0 and every KV head h,
+ * with row = (s / page_size * num_kv_heads + h) * page_size + s % page_size:
+ *   scale = max_d |x[d]| / 448 in fp32 (448 being the largest finite e4m3fn value),
+ *   code[d] = x[d] / scale taken as the fp32 product x[d] * (448 / amax), the reciprocal
+ *   rounded to fp32 once per row (the fp32 quotient where it overflows), then rounded to
+ *   the nearest e4m3fn value (ties to even) and saturated to +-448 (all codes 0 when
+ *   amax is 0),
+ *   k_scale[row] = scale, k_cache[row][d] = code[d]; V the same.
+ * Inputs must be finite (codes of NaN or infinite inputs are unspecified).  Slots past
+ * the cache are skipped and reported through *status.  Rows of different tokens must
+ * not share a slot.  One kernel launch on `stream`; no host synchronisation, no
+ * allocation.  Returns PA_ERR_INVALID_ARG for a missing pointer or a bad size (also
+ * num_tokens * num_kv_heads above 2^31 - 1), PA_ERR_ALIGN for a misaligned pointer,
+ * PA_ERR_UNSUPPORTED for head_dim or page_size outside the list, PA_ERR_CUDA when the
+ * launch fails. */
+pa_status_t pa_kv_quantize_write(const pa_kv_write_args_t *args, void *stream);
 
 /* ---- test hooks: exact integer / byte outputs of the row map and the page gather ---- */
 

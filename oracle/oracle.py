@@ -68,6 +68,13 @@ class OracleLib:
         lib.oracle_key_positions.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int,
                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_key_positions.restype = ctypes.c_int64
+        lib.oracle_enc_e4m3.argtypes = [ctypes.c_double]
+        lib.oracle_enc_e4m3.restype = ctypes.c_uint8
+        lib.oracle_kv_quantize_write.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_kv_quantize_write.restype = ctypes.c_int64
         self.lib = lib
         self.path = path
 
@@ -104,6 +111,22 @@ class OracleLib:
 
     def dec_bf16(self, bits: int) -> float:
         return float(self.lib.oracle_dec_bf16(int(bits)))
+
+    def enc_e4m3(self, x: float) -> int:
+        return int(self.lib.oracle_enc_e4m3(float(x)))
+
+    def kv_quantize_write(self, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+        """Per-token e4m3 quantisation of new K/V rows (bf16 bit patterns [T, Hkv, D]) into
+        the paged cache arrays, in place; returns the number of out-of-range slots."""
+        T, Hkv, D = k_new.shape
+        P, _, ps, _ = k_cache.shape
+        for a, dt in ((k_new, np.uint16), (v_new, np.uint16), (k_cache, np.uint8),
+                      (v_cache, np.uint8), (k_scale, np.float32), (v_scale, np.float32)):
+            assert a.dtype == dt and a.flags.c_contiguous
+        sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        return int(self.lib.oracle_kv_quantize_write(
+            k_new.ctypes.data, v_new.ctypes.data, sm.ctypes.data, T, Hkv, D, ps, P,
+            k_cache.ctypes.data, v_cache.ctypes.data, k_scale.ctypes.data, v_scale.ctypes.data))
 
 
 def build_variant(source_text: str, out_path: str) -> str:
@@ -183,6 +206,15 @@ def dec_e4m3(code: int) -> float:
 
 def dec_bf16(bits: int) -> float:
     return default().dec_bf16(bits)
+
+
+def enc_e4m3(x: float) -> int:
+    return default().enc_e4m3(x)
+
+
+def kv_quantize_write(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+    return default().kv_quantize_write(k_new, v_new, slot_mapping, k_cache, v_cache,
+                                       k_scale, v_scale)
 
 
 def row_map(cu_seqlens_q, context_lens):

@@ -284,3 +284,99 @@ int64_t oracle_key_positions(const oracle_problem *pb, int r, int tok, int64_t *
   if (need > cap) return -1;
   return key_set(pb, r, tok, keys);
 }
+
+/* ------------------------------------------------------------------------------------
+ * KV quantise-and-write: the producer of the per-token FP8 cache that the decode reads
+ * (ROCm/ATOM PR 2614: MiniMax-M3 writes FP8 KV plus per-token K/V scales, and the
+ * "Validation" section runs a producer-to-consumer operator test; the cache-write branch
+ * of ATOM PR 2710, "Smaller").
+ *
+ * For every new token t whose slot s = slot_mapping[t] is >= 0 and every KV head h:
+ *   page = s / page_size, o = s % page_size, row = (page * Hkv + h) * page_size + o;
+ *   x = the token's head_dim values (bf16, read exactly);
+ *   amax = max |x| and scale = amax / 448 (448: largest finite e4m3fn value), in fp32;
+ *   code[d] = e4m3 of x[d] / scale, taken as the fp32 product x[d] * (448 / amax) with
+ *   the reciprocal rounded to fp32 once per row (the fp32 quotient x[d] / scale where
+ *   that reciprocal overflows), rounded to nearest, ties to an even mantissa, and
+ *   saturated to +-448; all zero when amax = 0;
+ *   k_scale[row] = scale, k_cache[row * D + d] = code[d] (V the same).
+ * The fp32 steps are the decisions a code depends on, so they are taken in fp32 here
+ * as in the kernel; the rounding to e4m3 is exact arithmetic on that fp32 quotient.
+ * Slots >= num_pages * page_size are skipped and counted in the return value.
+ * ------------------------------------------------------------------------------------ */
+
+/* Nearest e4m3fn code to the real value x (ties to even mantissa), saturating to +-448.
+ * NaN gives the NaN code 0x7F. */
+uint8_t oracle_enc_e4m3(double x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: multiples of 2^-9; m = 8 is the smallest normal, code 0x08 */
+    double m = nearbyint(ldexp(a, 9));  /* current rounding mode: to nearest, ties even */
+    return sign | (uint8_t)m;
+  }
+  int e;
+  (void)frexp(a, &e);  /* a = f * 2^e, f in [0.5, 1) -> a in [2^(e-1), 2^e) */
+  int ex = e - 1;      /* unbiased exponent, -6 .. 8 */
+  double m = nearbyint((ldexp(a, -ex) - 1.0) * 8.0);  /* exact: a has 24 significant bits */
+  if (m == 8.0) {
+    m = 0.0;
+    ++ex;
+  }
+  if (ex > 8 || (ex == 8 && m > 6.0)) return sign | 0x7E;  /* above 448: saturate */
+  return sign | (uint8_t)(((ex + 7) << 3) | (int)m);
+}
+
+static float bf16_to_f32(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static void quantize_row(const uint16_t *x, int D, uint8_t *code, float *scale) {
+  float amax = 0.0f;
+  for (int d = 0; d < D; ++d) {
+    float a = fabsf(bf16_to_f32(x[d]));
+    if (a > amax) amax = a;
+  }
+  volatile float s = amax / 448.0f;  /* one fp32 division, stored as fp32 */
+  *scale = s;
+  /* the division by the scale, as a product with the fp32 reciprocal 448 / amax (the
+     quotient itself where that reciprocal overflows, amax below about 1.3e-36) */
+  volatile float inv = 448.0f / amax;
+  for (int d = 0; d < D; ++d) {
+    if (amax == 0.0f) {
+      code[d] = 0;
+      continue;
+    }
+    volatile float q = isinf(inv) ? bf16_to_f32(x[d]) / s : bf16_to_f32(x[d]) * inv;
+    code[d] = oracle_enc_e4m3((double)q);  /* the fp32 value that decides the code */
+  }
+}
+
+int64_t oracle_kv_quantize_write(const uint16_t *k_new, const uint16_t *v_new,
+                                 const int64_t *slot_mapping, int64_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                 int64_t num_pages, uint8_t *k_cache, uint8_t *v_cache,
+                                 float *k_scale, float *v_scale) {
+  int64_t bad = 0;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    if (s < 0) continue;
+    if (s >= num_pages * page_size) {
+      ++bad;
+      continue;
+    }
+    const int64_t page = s / page_size, o = s % page_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const int64_t row = (page * num_kv_heads + h) * page_size + o;
+      const int64_t src = (t * num_kv_heads + h) * head_dim;
+      quantize_row(k_new + src, head_dim, k_cache + row * head_dim, k_scale + row);
+      quantize_row(v_new + src, head_dim, v_cache + row * head_dim, v_scale + row);
+    }
+  }
+  return bad;
+}

@@ -65,6 +65,18 @@ class PlanInfo(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class KvWriteArgs(ctypes.Structure):
+    _fields_ = [("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("slot_mapping", ctypes.c_void_p), ("k_cache", ctypes.c_void_p),
+                ("v_cache", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("num_tokens", ctypes.c_int64), ("num_pages", ctypes.c_int64),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+DEV_BAD_SLOT = 0x100
+
 _lib = None
 P = ctypes.c_void_p
 
@@ -112,6 +124,8 @@ def lib(path: Optional[str] = None):
     L.pa_debug_gather.restype = ctypes.c_int
     L.pa_decode_noalloc.argtypes = [ctypes.POINTER(PlanDesc), ctypes.POINTER(DecodeArgs), P]
     L.pa_decode_noalloc.restype = ctypes.c_int
+    L.pa_kv_quantize_write.argtypes = [ctypes.POINTER(KvWriteArgs), P]
+    L.pa_kv_quantize_write.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -281,3 +295,34 @@ class Plan:
         if st != 0:
             raise PaError(st, "pa_debug_gather")
         return dump, tb
+
+
+def kv_write_args(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale, status=None,
+                  num_tokens=None) -> KvWriteArgs:
+    """pa_kv_write_args_t over torch tensors: k_new / v_new bf16 [T, Hkv, D], slot_mapping
+    int64 [T], caches uint8 [num_pages, Hkv, page_size, D], scales fp32
+    [num_pages, Hkv, page_size], status an optional int32/uint32 device word."""
+    a = KvWriteArgs()
+    a.k_new, a.v_new, a.slot_mapping = _ptr(k_new), _ptr(v_new), _ptr(slot_mapping)
+    a.k_cache, a.v_cache, a.k_scale, a.v_scale = (_ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                                  _ptr(v_scale))
+    a.status = _ptr(status)
+    a.num_tokens = int(num_tokens if num_tokens is not None else k_new.shape[0])
+    a.num_pages = int(k_cache.shape[0])
+    a.num_kv_heads = int(k_cache.shape[1])
+    a.page_size = int(k_cache.shape[2])
+    a.head_dim = int(k_cache.shape[3])
+    a.reserved = 0
+    return a
+
+
+def kv_quantize_write(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                      status=None, stream=None, args: Optional[KvWriteArgs] = None) -> None:
+    """Enqueues pa_kv_quantize_write on `stream` (default: torch's current stream)."""
+    import torch
+    a = args if args is not None else kv_write_args(k_new, v_new, slot_mapping, k_cache, v_cache,
+                                                    k_scale, v_scale, status)
+    s = stream if stream is not None else torch.cuda.current_stream(k_cache.device)
+    st = lib().pa_kv_quantize_write(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
+    if st != 0:
+        raise PaError(st, "pa_kv_quantize_write")

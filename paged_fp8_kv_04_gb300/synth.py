@@ -265,6 +265,71 @@ def sparse_selected(seed: int = 4, num_seqs: int = 32, context: int = 131072,
                         only_selected_data=only_selected_data, name="sparse selected-page decode")
 
 
+@dataclasses.dataclass
+class KvWriteCase:
+    """New K/V rows (bf16 bits [T, Hkv, D]), their slots, and sentinel-filled caches."""
+    k_new: np.ndarray
+    v_new: np.ndarray
+    slot_mapping: np.ndarray      # int64 [T]
+    k_cache: np.ndarray           # uint8 [P, Hkv, ps, D]
+    v_cache: np.ndarray
+    k_scale: np.ndarray           # fp32 [P, Hkv, ps]
+    v_scale: np.ndarray
+    name: str = ""
+
+
+def kv_write_case(seed: int, num_tokens: int, num_kv_heads: int = 1, page_size: int = 128,
+                  num_pages: int = 64, skip: int = 0, past_end: int = 0,
+                  special_rows: bool = True, name: str = "") -> KvWriteCase:
+    """Seeded new-token K/V rows for the quantise-and-write step.
+
+    Rows are N(0, 1) times a per-row magnitude drawn log-uniformly from 2^-20 .. 2^20;
+    with special_rows, a few rows are all zero, e4m3 values times a power of two (with
+    +-448 among them), or one nonzero value, and one row mixes magnitudes 2^-40 .. 2^10.
+    Slots are distinct and drawn without replacement from the cache; `skip` tokens get
+    slot -1 and `past_end` tokens a slot past the cache.  Caches hold sentinel bytes."""
+    rng = np.random.default_rng(seed)
+    T, Hkv, D, ps, P = num_tokens, num_kv_heads, 128, page_size, num_pages
+    assert T <= P * ps
+    mag = np.exp2(rng.uniform(-20, 20, size=(T, Hkv, 1))).astype(np.float32)
+    x = (_normal(rng, (T, Hkv, D)) * mag).astype(np.float32)
+    y = (_normal(rng, (T, Hkv, D)) * mag[::-1]).astype(np.float32)
+    if special_rows and T >= 4:
+        x[0, 0] = 0.0
+        codes = rng.integers(0, 0x7F, size=D).astype(np.uint8) | \
+            (rng.integers(0, 2, size=D).astype(np.uint8) << 7)
+        codes[codes & 0x7F == 0x7F] = 0x7E
+        codes[5] = 0x7E
+        x[1, 0] = e4m3_values(codes) * np.float32(2.0 ** -7)
+        y[2, 0] = 0.0
+        y[2, 0, 77] = np.float32(-0.3125)
+        x[3, 0] = (_normal(rng, (D,)) * np.exp2(rng.uniform(-40, 10, size=D))).astype(np.float32)
+    slots = rng.choice(P * ps, size=T, replace=False).astype(np.int64)
+    idx = rng.permutation(T)
+    slots[idx[:skip]] = -1
+    slots[idx[skip:skip + past_end]] = P * ps + rng.integers(0, 1000, size=past_end)
+    return KvWriteCase(
+        k_new=bf16_bits(x), v_new=bf16_bits(y), slot_mapping=slots,
+        k_cache=np.full((P, Hkv, ps, D), 0xC3, dtype=np.uint8),
+        v_cache=np.full((P, Hkv, ps, D), 0x3C, dtype=np.uint8),
+        k_scale=np.full((P, Hkv, ps), -1.0, dtype=np.float32),
+        v_scale=np.full((P, Hkv, ps), -2.0, dtype=np.float32), name=name)
+
+
+def kv_write_prefill_8k(seed: int = 5) -> KvWriteCase:
+    """The whole dense-8K batch written at once: 32 sequences x 8192 tokens = 262144 tokens,
+    Hkv 1, page 128, into a 2048-page pool.  Each sequence owns 64 pages of a random
+    permutation of the pool (its block table) and its tokens fill them in order, as a
+    prefill writes them."""
+    c = kv_write_case(seed, 32 * 8192, 1, 128, 2048, special_rows=True,
+                      name="KV quantise-and-write, 262144 tokens (dense 8K batch)")
+    rng = np.random.default_rng(seed + 77)
+    pages = rng.permutation(2048).astype(np.int64).reshape(32, 64)
+    pos = np.arange(8192, dtype=np.int64)
+    c.slot_mapping = (pages[:, pos // 128] * 128 + pos % 128).reshape(-1)
+    return c
+
+
 def kv_bytes_per_token(p: Problem) -> int:
     """Algorithmic bytes of one attended (token, KV head): K and V rows plus scales."""
     if p.kv_dtype == "bf16":

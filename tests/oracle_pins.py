@@ -388,4 +388,156 @@ def pin_golden_q_shape_225280(lib):
     assert o.shape == (110, 16, 128)
 
 
+# ---------------------------------------------------------- KV quantise-and-write (producer)
+
+def _finite_code_values():
+    """Values of the 254 finite e4m3fn codes, through torch's decoding (pinned above)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    fin = ~np.isnan(vals)
+    return np.arange(256)[fin], vals[fin]
+
+
+def _brute_nearest_code(x, codes, vals):
+    """Nearest finite code of x's sign by exhaustive search; ties go to the even code."""
+    if abs(x) > 448.0:
+        return 0x7E | (0x80 if x < 0 else 0)
+    neg = np.signbit(x)
+    m = ((codes & 0x80) != 0) == neg
+    c, v = codes[m], vals[m]
+    d = np.abs(v - x)
+    best = d.min()
+    cand = c[d == best]
+    even = cand[(cand & 1) == 0]
+    return int(even[0] if even.size else cand[0])
+
+
+def _encode_probe_values():
+    codes, vals = _finite_code_values()
+    pos = np.unique(vals[vals >= 0])
+    mids = (pos[:-1] + pos[1:]) / 2                       # exact ties
+    ulp = np.spacing(mids.astype(np.float32)).astype(np.float64)
+    rng = np.random.default_rng(11)
+    rand = np.exp2(rng.uniform(-12, 9.2, 3000)).astype(np.float32).astype(np.float64)
+    xs = np.concatenate([pos, mids, mids - ulp, mids + ulp, rand, [449.0, 463.9, 1e6]])
+    xs = xs.astype(np.float32).astype(np.float64)
+    return np.concatenate([xs, -xs])
+
+
+def pin_e4m3_encode_is_nearest(lib):
+    """The encoder returns the nearest e4m3fn code (ties to even, saturating at 448),
+    checked by exhaustive search over the 254 finite codes."""
+    codes, vals = _finite_code_values()
+    for x in _encode_probe_values():
+        want = _brute_nearest_code(float(x), codes, vals)
+        got = lib.enc_e4m3(float(x))
+        assert got == want, f"enc({x!r}) = {got:#x}, nearest is {want:#x}"
+
+
+def pin_e4m3_encode_matches_torch(lib):
+    """Within [-464, 464] the encoder agrees with torch's float32 -> float8_e4m3fn cast."""
+    xs = _encode_probe_values()
+    xs = xs[np.abs(xs) <= 464.0]
+    ref = torch.from_numpy(xs.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    got = np.array([lib.enc_e4m3(float(x)) for x in xs], dtype=np.uint8)
+    assert np.array_equal(got, ref.numpy()), "encoder differs from torch's cast"
+
+
+def _kv_case(T=6, Hkv=2, D=128, ps=16, P=5, seed=21):
+    rng = np.random.default_rng(seed)
+    k = synth.bf16_bits(rng.standard_normal((T, Hkv, D)).astype(np.float32) * 3)
+    v = synth.bf16_bits(rng.standard_normal((T, Hkv, D)).astype(np.float32) * 0.01)
+    kc = np.full((P, Hkv, ps, D), 0xA5, dtype=np.uint8)
+    vc = np.full((P, Hkv, ps, D), 0x5A, dtype=np.uint8)
+    ks = np.full((P, Hkv, ps), -7.0, dtype=np.float32)
+    vs = np.full((P, Hkv, ps), -9.0, dtype=np.float32)
+    return k, v, kc, vc, ks, vs
+
+
+def _bf16_of(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def pin_quantize_write_closed_forms(lib):
+    """Closed forms of the per-token quantiser and the slot placement:
+    - a row of e4m3 values times a power of two, whose largest magnitude is 448 times it,
+      comes back as exactly those codes, with that power of two as its scale;
+    - an all-zero row gives scale 0 and zero codes;
+    - a row with one nonzero value a gives scale |a| / 448 (fp32) and the code of +-448;
+    - slot s lands at page s // page_size, offset s % page_size, for every KV head; a slot
+      of -1 and a slot past the cache change nothing, and the latter is counted."""
+    T, Hkv, D, ps, P = 6, 2, 128, 16, 5
+    k, v, kc, vc, ks, vs = _kv_case(T, Hkv, D, ps, P)
+    codes, vals = _finite_code_values()
+    rng = np.random.default_rng(5)
+    exact_codes = rng.choice(codes[np.abs(vals) < 448], size=D).astype(np.uint8)
+    exact_codes[17] = 0xFE                                # -448 somewhere in the row
+    s = 2.0 ** -5
+    row = np.array([lib.dec_e4m3(int(c)) for c in exact_codes]) * s
+    k[0, 1] = synth.bf16_bits(row.astype(np.float32))
+    k[1, 0] = 0
+    one = np.zeros(D, dtype=np.float32)
+    one[40] = -3.140625                                   # bf16-exact
+    v[2, 1] = synth.bf16_bits(one)
+    # exact midpoints between neighbouring e4m3 values (times 2^-7, with 448 * 2^-7 as the
+    # row maximum): the quotient is the midpoint itself, so each code is the even neighbour
+    pos = np.unique(vals[(vals > 0) & (vals < 448)])
+    mids = ((pos[:-1] + pos[1:]) / 2)[::3][:D - 1]
+    mid_row = np.zeros(D, dtype=np.float64)
+    mid_row[:mids.size] = mids * np.where(np.arange(mids.size) % 2 == 0, 1.0, -1.0)
+    mid_row[D - 1] = 448.0
+    mid_codes = np.array([_brute_nearest_code(float(x), codes, vals) for x in mid_row], np.uint8)
+    k[5, 0] = synth.bf16_bits((mid_row * 2.0 ** -7).astype(np.float32))
+    assert np.array_equal(_bf16_of(k[5, 0]).astype(np.float64), mid_row * 2.0 ** -7)
+    slots = np.array([3 * ps + 7, 0, 4 * ps + ps - 1, -1, P * ps + 2, ps + 1], dtype=np.int64)
+    kc0, vc0, ks0, vs0 = kc.copy(), vc.copy(), ks.copy(), vs.copy()
+    bad = lib.kv_quantize_write(k, v, slots, kc, vc, ks, vs)
+    assert bad == 1, "the slot past the cache is not counted"
+    # token 0, head 1: exact codes and scale
+    assert np.array_equal(kc[3, 1, 7], exact_codes), "exact e4m3 row not reproduced"
+    assert ks[3, 1, 7] == np.float32(s), "power-of-two scale not reproduced"
+    # token 1, head 0: zero row
+    assert ks[0, 0, 0] == 0.0 and not kc[0, 0, 0].any(), "zero row"
+    # token 5, head 0: midpoints go to the even neighbour
+    assert np.array_equal(kc[1, 0, 1], mid_codes), "ties not rounded to the even code"
+    # token 2, head 1: one nonzero V value
+    assert vs[4, 1, ps - 1] == np.float32(np.float32(3.140625) / np.float32(448.0))
+    want = np.zeros(D, dtype=np.uint8)
+    want[40] = 0xFE
+    assert np.array_equal(vc[4, 1, ps - 1], want), "single-value row"
+    # placement: exactly the rows of the written slots changed
+    written = {(3, 7), (0, 0), (4, ps - 1), (1, 1)}
+    for pg in range(P):
+        for o in range(ps):
+            for h in range(Hkv):
+                same = (np.array_equal(kc[pg, h, o], kc0[pg, h, o]) and
+                        np.array_equal(vc[pg, h, o], vc0[pg, h, o]) and
+                        ks[pg, h, o] == ks0[pg, h, o] and vs[pg, h, o] == vs0[pg, h, o])
+                assert same == ((pg, o) not in written), f"placement at page {pg} slot {o}"
+
+
+def pin_quantize_write_round_trip(lib):
+    """Dequantised codes (code value x scale) lie within half an e4m3 step of the input,
+    every row's largest magnitude maps to +-448, and K and V rows are kept apart."""
+    T, Hkv, D, ps, P = 6, 2, 128, 16, 5
+    k, v, kc, vc, ks, vs = _kv_case(T, Hkv, D, ps, P, seed=33)
+    slots = np.arange(T, dtype=np.int64) * 3 + 1
+    lib.kv_quantize_write(k, v, slots, kc, vc, ks, vs)
+    dec = np.array([lib.dec_e4m3(c) if c not in (0x7F, 0xFF) else np.nan for c in range(256)])
+    for t in range(T):
+        pg, o = divmod(int(slots[t]), ps)
+        for h in range(Hkv):
+            for new, cache, sc in ((k, kc, ks), (v, vc, vs)):
+                x = _bf16_of(new[t, h]).astype(np.float64)
+                scale = float(sc[pg, h, o])
+                y = dec[cache[pg, h, o]] * scale
+                amax = np.abs(x).max()
+                assert np.isclose(scale, amax / 448.0, rtol=2 ** -23), "scale is not amax / 448"
+                assert abs(np.abs(y).max() - amax) <= amax * 2 ** -20, "amax element not at 448"
+                # e4m3 has 3 mantissa bits: error <= 2^-4 relative, or half a subnormal step
+                err = np.abs(y - x)
+                bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * scale) * (1 + 1e-6)
+                assert np.all(err <= bound), "dequantised value too far from the input"
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

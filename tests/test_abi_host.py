@@ -247,3 +247,38 @@ def test_noalloc_refuses_a_plan_larger_than_its_scratch(lib):
     call = FakeCall(2, 2, cu_seqlens_q=0x9000000)
     assert lib.pa_decode_noalloc(ctypes.byref(big), ctypes.byref(call.a), None) == CAP
     assert lib.pa_decode_noalloc(None, ctypes.byref(call.a), None) == INVALID
+
+
+def _kv_args(**over):
+    a = B.KvWriteArgs()
+    vals = dict(k_new=0x100000, v_new=0x200000, slot_mapping=0x300000, k_cache=0x400000,
+                v_cache=0x500000, k_scale=0x600000, v_scale=0x700000, status=None,
+                num_tokens=0, num_pages=8, num_kv_heads=1, head_dim=128, page_size=128,
+                reserved=0)
+    vals.update(over)
+    for k, v in vals.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_kv_quantize_write_refusals(lib):
+    """pa_kv_quantize_write checks its arguments before touching a device; with no
+    tokens a valid call enqueues nothing and succeeds."""
+    call = lambda **kw: lib.pa_kv_quantize_write(ctypes.byref(_kv_args(**kw)), None)
+    assert lib.pa_kv_quantize_write(None, None) == INVALID
+    assert call() == OK
+    assert call(head_dim=64) == UNSUP
+    assert call(page_size=48) == UNSUP
+    assert call(page_size=256) == UNSUP
+    assert call(num_tokens=-1) == INVALID
+    assert call(num_kv_heads=0) == INVALID
+    assert call(num_pages=0) == INVALID
+    assert call(reserved=3) == INVALID
+    assert call(num_tokens=1 << 30, num_kv_heads=4) == INVALID
+    assert call(k_new=None) == INVALID
+    assert call(v_scale=None) == INVALID
+    assert call(k_new=0x100008) == ALIGN
+    assert call(v_cache=0x500004) == ALIGN
+    assert call(k_scale=0x600002) == ALIGN
+    assert call(slot_mapping=0x300004) == ALIGN
+    assert call(status=0x800002) == ALIGN

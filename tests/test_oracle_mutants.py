@@ -33,6 +33,21 @@ MUTANTS = {
                          "const int64_t row = row0 + (qlen - 1 - tok);"),
     "lse_without_max": ("smax + log(z)", "log(z)"),
     "softmax_sign": ("exp(scores[j] - smax)", "exp(smax - scores[j])"),
+    "enc_ties_away": ("double m = nearbyint((ldexp(a, -ex) - 1.0) * 8.0);",
+                      "double m = round((ldexp(a, -ex) - 1.0) * 8.0);"),
+    "enc_truncates": ("double m = nearbyint((ldexp(a, -ex) - 1.0) * 8.0);",
+                      "double m = floor((ldexp(a, -ex) - 1.0) * 8.0);"),
+    "enc_subnormal_step": ("double m = nearbyint(ldexp(a, 9));",
+                           "double m = nearbyint(ldexp(a, 8));"),
+    "enc_no_saturation": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 480.0) return sign | 0x7F;"),
+    "quant_scale_447": ("volatile float s = amax / 448.0f;", "volatile float s = amax / 447.0f;"),
+    "quant_inv_447": ("volatile float inv = 448.0f / amax;", "volatile float inv = 447.0f / amax;"),
+    "quant_slot_offset": ("const int64_t page = s / page_size, o = s % page_size;",
+                          "const int64_t page = s / page_size, o = (s + 1) % page_size;"),
+    "quant_head_stride": ("const int64_t row = (page * num_kv_heads + h) * page_size + o;",
+                          "const int64_t row = (page * num_kv_heads) * page_size + o;"),
+    "quant_v_from_k": ("quantize_row(v_new + src,", "quantize_row(k_new + src,"),
+    "quant_skips_counted": ("      ++bad;\n      continue;", "      continue;"),
 }
 
 
