@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dense8k",
                     choices=["dense8k", "bf16ctl", "long128k_scalar", "long128k", "ragged",
-                             "sparse", "kv_write"])
+                             "sparse", "kv_write", "prefill"])
     ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = balanced)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -92,6 +92,14 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def make_workload(name):
     from paged_fp8_kv_04_gb300 import synth
     if name == "dense8k":
@@ -107,6 +115,11 @@ def make_workload(name):
     elif name == "long128k":
         p = synth.long_128k(2, scale_mode="per_token")
         desc = "long-context decode 128K: batch 8, context 131072, q_len 1, per-token e4m3 scales"
+    elif name == "prefill":
+        p = synth.prefill_as_decode(6, 2048, 6144)
+        desc = ("per-token-as-decode prefill: a 2048-token chunk after 6144 prompt tokens of one "
+                "sequence, 2048 requests of q_len 1 sharing its block table, page 128, per-token "
+                "e4m3 K/V")
     elif name == "ragged":
         p = synth.ragged_spec(3, "A")
         desc = "ragged speculative decode: 31 requests (30 x q_len 4 + 1 x q_len 1, 121 rows)"
@@ -466,6 +479,17 @@ def bench_ours(args):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clk,
         "device_flags": flags,
     }
+    if args.workload == "prefill":
+        # The rows share one sequence's pages, so the attended bytes come from L2 many
+        # times over: the bound is the contraction, 4 * D * g flops per attended token.
+        flops = 4 * p.head_dim * p.group_size * p.num_kv_heads * int(p.context_lens.astype(np.int64).sum())
+        tf = flops / (us_per_call * 1e-6) / 1e12
+        tpeak = tensor_peak()
+        line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
+                            "frac": tf / tpeak, "traffic": None,
+                            "peak_kind": "measured bf16_tflops (cuBLAS burst); f16 mma.sync runs below it"}
+        line["attended_bytes_per_s_note"] = "value counts attended KV bytes, most served from L2"
+        line["tokens_per_s"] = rows_s
     print(json.dumps(line), flush=True)
 
 
@@ -494,6 +518,14 @@ def bench_kv_write(args, dev, rank, world, local):
     total_bytes = kv_write_bytes(c)
     alist = [B.kv_write_args(k, v, slots, kc, vc, ks, vs) for k, v in ins]
     stream = torch.cuda.Stream(device=dev)
+    if args.profile:
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.profile):
+                B.kv_quantize_write(None, None, None, kc, None, None, None, stream=stream,
+                                    args=alist[i % 2])
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_calls": args.warmup + args.profile}), flush=True)
+        return
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             B.kv_quantize_write(None, None, None, kc, None, None, None, stream=stream,

@@ -20,7 +20,6 @@ constexpr int kUnits = 4;          // (token, KV head) rows per warp step
 constexpr int kWarps = 8;          // warps per CTA
 constexpr float kE4m3Max = 448.f;  // largest finite e4m3fn value
 constexpr bool kPipe = true;      // next step's loads before this step's arithmetic
-constexpr int kCtasPerSm = 3;     // one wave of resident CTAs
 
 struct KvWriteParams {
   const uint16_t *k_new, *v_new;
@@ -111,10 +110,14 @@ __device__ __forceinline__ void quantize_step(const KvWriteParams &p, const Step
     uint4 codes = make_uint4(0, 0, 0, 0);
     if (amax != 0.f) {
       const float inv = __fdiv_rn(kE4m3Max, amax);
-      const bool big = isinf(inv);
       float q[16];
+      if (!isinf(inv)) {
 #pragma unroll
-      for (int d = 0; d < 16; ++d) q[d] = big ? __fdiv_rn(x[d], scale) : __fmul_rn(x[d], inv);
+        for (int d = 0; d < 16; ++d) q[d] = __fmul_rn(x[d], inv);
+      } else {
+#pragma unroll
+        for (int d = 0; d < 16; ++d) q[d] = __fdiv_rn(x[d], scale);
+      }
       codes.x = pack4_e4m3(q[0], q[1], q[2], q[3]);
       codes.y = pack4_e4m3(q[4], q[5], q[6], q[7]);
       codes.z = pack4_e4m3(q[8], q[9], q[10], q[11]);
@@ -202,13 +205,27 @@ extern "C" pa_status_t pa_kv_quantize_write(const pa_kv_write_args_t *a, void *s
   p.Hkv = a->num_kv_heads;
   p.ps_shift = shift;
 
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return PA_ERR_CUDA;
+  // SMs and resident CTAs per SM, looked up once per device
+  static int cached[64][2];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  int sms = 0, per_sm = 0;
+  if (dev >= 0 && dev < 64 && cached[dev][0] > 0) {
+    sms = cached[dev][0];
+    per_sm = cached[dev][1];
+  } else {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_quantize_write_kernel<kPipe>,
+                                                      kWarps * 32, 0) != cudaSuccess)
+      return PA_ERR_CUDA;
+    if (dev >= 0 && dev < 64) {
+      cached[dev][1] = per_sm;
+      cached[dev][0] = sms;
+    }
+  }
   const int64_t groups = (p.units + kUnits - 1) / kUnits;
   const int64_t want = (groups + kWarps - 1) / kWarps;
-  const int64_t cap = (int64_t)sms * kCtasPerSm;
+  const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);  // one wave of resident CTAs
   const int grid = (int)(want < cap ? want : cap);
   kv_quantize_write_kernel<kPipe><<<grid, kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -265,6 +265,41 @@ def sparse_selected(seed: int = 4, num_seqs: int = 32, context: int = 131072,
                         only_selected_data=only_selected_data, name="sparse selected-page decode")
 
 
+def prefill_as_decode(seed: int = 6, num_tokens: int = 2048, prefix: int = 0,
+                      page_size: int = 128, selected_pages: Optional[int] = None,
+                      scale_mode: str = "per_token", name: str = "") -> Problem:
+    """A prefill chunk of one sequence run through the decode contract, one request per new
+    token (ROCm/ATOM PR 2614, "Change": per-token-as-decode prefill reuses the paged-decode
+    contract).  The sequence holds prefix + num_tokens tokens; request t is the query row of
+    token prefix + t, with context prefix + t + 1 and q_len 1, and every request shares the
+    sequence's block table, so row t attends exactly the causal prefix of its token.  With
+    selected_pages, request t attends that many of its prefix's pages instead (always its
+    own last page), as the sparse prefill does."""
+    L = prefix + num_tokens
+    base = make_problem(seed, num_seqs=1, context_lens=[L], q_lens=[1], page_size=page_size,
+                        scale_mode=scale_mode, name=name or "prefill as decode")
+    rng = np.random.default_rng(seed + 500)
+    T = num_tokens
+    ctx = (prefix + np.arange(1, T + 1)).astype(np.int32)
+    bt = np.repeat(base.block_table, T, axis=0)
+    q = bf16_bits(_normal(rng, (T, base.num_kv_heads * base.group_size, base.head_dim)))
+    sel = nsel = None
+    if selected_pages is not None:
+        sel = np.full((T, selected_pages), -1, dtype=np.int32)
+        nsel = np.zeros(T, dtype=np.int32)
+        for t in range(T):
+            n = (int(ctx[t]) + page_size - 1) // page_size
+            k = min(selected_pages, n)
+            others = rng.choice(n - 1, size=k - 1, replace=False) if k > 1 else np.zeros(0, int)
+            pick = np.concatenate([others, [n - 1]]).astype(np.int32)
+            rng.shuffle(pick)
+            sel[t, :k] = pick
+            nsel[t] = k
+    return dataclasses.replace(base, num_seqs=T, q=q, block_table=bt, context_lens=ctx,
+                               cu_seqlens_q=np.arange(T + 1, dtype=np.int32), uniform_q_len=1,
+                               selected=sel, num_selected=nsel)
+
+
 @dataclasses.dataclass
 class KvWriteCase:
     """New K/V rows (bf16 bits [T, Hkv, D]), their slots, and sentinel-filled caches."""

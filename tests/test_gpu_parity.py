@@ -359,3 +359,24 @@ def test_cuda_graph_capture_and_replay():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+# ------------------------------------------------- many rows: per-token-as-decode prefill
+
+def test_prefill_as_decode_dense():
+    """A 300-token prefill chunk after 100 prompt tokens, one request per token sharing the
+    sequence's pages: every row against the oracle (each attends its causal prefix)."""
+    check_against_oracle(synth.prefill_as_decode(6, 300, 100, page_size=16),
+                         what="prefill as decode")
+
+
+def test_prefill_as_decode_sparse():
+    """The sparse prefill: each token's request attends 8 of its prefix's pages."""
+    check_against_oracle(synth.prefill_as_decode(7, 200, 2000, page_size=16, selected_pages=8),
+                         what="sparse prefill as decode")
+
+
+def test_prefill_as_decode_full_size_sampled():
+    """The bench's prefill workload (2048 tokens after 6144), sampled rows."""
+    check_against_oracle(synth.prefill_as_decode(6, 2048, 6144), sample=[0, 1, 1023, 2047],
+                         what="prefill 2K after 6K")
