@@ -55,10 +55,11 @@ def parse():
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the decode kernel
 # from one ncu capture per workload, valid only for the kernel sources they were taken on
-# (sha256 over the CUDA sources and the C header); any other source gives traffic null.
+# (sha256 over the C header and the decode kernels' translation unit); any other source
+# gives traffic null.
 MEASURED_TRAFFIC = {
-    "dense8k": {"bytes": 69465088 + 738304,
-                "csrc_sha256": "4f8c723fd83c57f3397f3658bb21d948f0dd60736622a1e2bc4ef6f298e2ab44",
+    "dense8k": {"bytes": 69464320 + 693760,
+                "csrc_sha256": "68cd066aaee732fa5b9250ed075613948eed8cd5ca682b94808a265df79ac4aa",
                 "profile": "profiles/decode_kernel_dense8k_full.md"},
 }
 
@@ -68,8 +69,29 @@ def csrc_sha256():
     h = hashlib.sha256()
     files = [os.path.join(ROOT, "include", "pa.h")]
     cdir = os.path.join(ROOT, "paged_fp8_kv_04_gb300", "csrc")
-    files += [os.path.join(cdir, f) for f in sorted(os.listdir(cdir)) if f.endswith((".cu", ".cuh"))]
+    # the decode kernels' translation unit (pa_api.cu and the headers it includes)
+    files += [os.path.join(cdir, f) for f in sorted(os.listdir(cdir))
+              if f.endswith(".cuh") or f == "pa_api.cu"]
     for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+# The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
+# Its DRAM writes at kernel end are below the bytes it writes: L2 still holds dirty lines
+# when the launch ends, and writes them back during the next one.
+MEASURED_TRAFFIC_KV_WRITE = {"bytes": 136345856 + 35392512,
+                             "src_sha256": "44b6bc93ea801a2fdccab4b373d71575d565ad97b1cc5c1577eff57bf0eabaa2",
+                             "profile": "profiles/kv_quantize_write_prefill8k_full.md"}
+
+
+def kv_write_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for f in (os.path.join(ROOT, "include", "pa.h"),
+              os.path.join(ROOT, "paged_fp8_kv_04_gb300", "csrc", "pa_kv_write.cu")):
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
@@ -609,7 +631,10 @@ def bench_kv_write(args, dev, rank, world, local):
                    "timed": "CUDA graph replay of back-to-back pa_kv_quantize_write calls"},
         "us_per_call_graph": us, "algorithmic_bytes_per_call": int(total_bytes),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": (MEASURED_TRAFFIC_KV_WRITE["bytes"]
+                                 if MEASURED_TRAFFIC_KV_WRITE["src_sha256"] == kv_write_sha256()
+                                 else None),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clk,
     }
