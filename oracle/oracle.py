@@ -40,6 +40,18 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _IndexProblem(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32), ("index_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32), ("topk", ctypes.c_int32),
+        ("num_pages", ctypes.c_int64),
+        ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("bt_stride", ctypes.c_int32),
+        ("context_lens", ctypes.c_void_p), ("cu_seqlens_q", ctypes.c_void_p),
+        ("sm_scale", ctypes.c_double),
+    ]
+
+
 def build(force: bool = False) -> str:
     """Compile pa_oracle.c (plain C, -O2, pthreads) if it is missing or stale."""
     with _lock:
@@ -75,6 +87,9 @@ class OracleLib:
                                                  ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
                                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_kv_quantize_write.restype = ctypes.c_int64
+        lib.oracle_index_topk.argtypes = [ctypes.POINTER(_IndexProblem), ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+        lib.oracle_index_topk.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -114,6 +129,35 @@ class OracleLib:
 
     def enc_e4m3(self, x: float) -> int:
         return int(self.lib.oracle_enc_e4m3(float(x)))
+
+    def index_topk(self, ip):
+        """Indexer block scores and top-k pages of an index problem (synth.IndexProblem):
+        (selected int32 [rows, topk], num_selected int32 [rows], scores fp64
+        [rows, max pages], -inf where a page is not a candidate)."""
+        R = int(ip.cu_seqlens_q[-1])
+        stride = max(int(ip.block_table.shape[1]), 1)
+        arrs = dict(q=np.ascontiguousarray(ip.q, dtype=np.uint16),
+                    k=np.ascontiguousarray(ip.k_cache, dtype=np.uint8),
+                    ks=None if ip.k_scale is None else np.ascontiguousarray(ip.k_scale, dtype=np.float32),
+                    bt=np.ascontiguousarray(ip.block_table, dtype=np.int32),
+                    L=np.ascontiguousarray(ip.context_lens, dtype=np.int32),
+                    cu=np.ascontiguousarray(ip.cu_seqlens_q, dtype=np.int32))
+        st = _IndexProblem(num_seqs=len(arrs["L"]), index_heads=ip.q.shape[1],
+                           head_dim=ip.q.shape[2], page_size=ip.k_cache.shape[1],
+                           topk=ip.topk, num_pages=ip.k_cache.shape[0],
+                           q=arrs["q"].ctypes.data, k_cache=arrs["k"].ctypes.data,
+                           k_scale=None if arrs["ks"] is None else arrs["ks"].ctypes.data,
+                           block_table=arrs["bt"].ctypes.data, bt_stride=stride,
+                           context_lens=arrs["L"].ctypes.data, cu_seqlens_q=arrs["cu"].ctypes.data,
+                           sm_scale=float(ip.sm_scale))
+        sel = np.zeros((R, max(ip.topk, 1)), dtype=np.int32)
+        nsel = np.zeros(R, dtype=np.int32)
+        scores = np.zeros((R, stride), dtype=np.float64)
+        rc = self.lib.oracle_index_topk(ctypes.byref(st), sel.ctypes.data, nsel.ctypes.data,
+                                        scores.ctypes.data, stride)
+        if rc != 0:
+            raise RuntimeError("oracle_index_topk failed")
+        return sel[:, :ip.topk], nsel, scores
 
     def kv_quantize_write(self, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
         """Per-token e4m3 quantisation of new K/V rows (bf16 bit patterns [T, Hkv, D]) into
@@ -210,6 +254,10 @@ def dec_bf16(bits: int) -> float:
 
 def enc_e4m3(x: float) -> int:
     return default().enc_e4m3(x)
+
+
+def index_topk(ip):
+    return default().index_topk(ip)
 
 
 def kv_quantize_write(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):

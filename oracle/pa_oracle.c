@@ -380,3 +380,94 @@ int64_t oracle_kv_quantize_write(const uint16_t *k_new, const uint16_t *v_new,
   }
   return bad;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Indexer block score and top-k page selection: the step that produces the selected
+ * pages of the sparse decode (ROCm/ATOM PR 2122, section 1: the index cache holds
+ * (num_blocks, 128, 128) e4m3 codes and the block-score kernel takes q . k scaled by
+ * sm_scale * log2(e); section 2: the index top-k maps rows to requests through
+ * cu_seqlens_q with the cutoff seq_len - q_len + tok + 1).
+ *
+ * For query row tok of request r (cutoff c = L - q_len + tok + 1, limit = min(L, c)):
+ *   s[h][p] = sm_scale * log2(e) * sum_d q[row][h][d] * K^[p][d], K^ = dec(code) * scale
+ *     (per-token index scale, or 1), for attended positions p < limit;
+ *   S[b] = log2( sum_h sum_{p in page b, p < limit} 2^s[h][p] ) for every page b holding
+ *     an attended position (the candidates);
+ *   selected[row] = the page holding position limit - 1 first, then the other candidates
+ *     by descending S (equal scores: lower page first), topk entries at most, -1 after;
+ *   num_selected[row] = their count.  S itself is returned too.
+ * ------------------------------------------------------------------------------------ */
+typedef struct oracle_index_problem {
+  int32_t num_seqs, index_heads, head_dim, page_size, topk;
+  int64_t num_pages;
+  const uint16_t *q;            /* [rows, index_heads, D] bf16 bits */
+  const uint8_t *k_cache;       /* [num_pages, page_size, D] e4m3 codes */
+  const float *k_scale;         /* [num_pages, page_size] or NULL */
+  const int32_t *block_table;   /* [num_seqs, bt_stride] */
+  int32_t bt_stride;
+  const int32_t *context_lens;
+  const int32_t *cu_seqlens_q;
+  double sm_scale;
+} oracle_index_problem;
+
+int oracle_index_topk(const oracle_index_problem *pb, int32_t *selected, int32_t *num_selected,
+                      double *scores, int32_t scores_stride) {
+  const int D = pb->head_dim, ps = pb->page_size, H = pb->index_heads;
+  const double log2e = 1.4426950408889634074;
+  for (int r = 0; r < pb->num_seqs; ++r) {
+    const int64_t L = pb->context_lens[r];
+    const int64_t row0 = pb->cu_seqlens_q[r], qlen = pb->cu_seqlens_q[r + 1] - row0;
+    for (int64_t tok = 0; tok < qlen; ++tok) {
+      const int64_t row = row0 + tok;
+      int64_t lim = L - qlen + tok + 1;
+      if (lim > L) lim = L;
+      if (lim < 0) lim = 0;
+      const int64_t nb = (lim + ps - 1) / ps;
+      if (nb > scores_stride) return -1;
+      double *S = scores + row * scores_stride;
+      for (int64_t b = 0; b < scores_stride; ++b) S[b] = -INFINITY;
+      for (int64_t b = 0; b < nb; ++b) {
+        const int64_t phys = pb->block_table[(int64_t)r * pb->bt_stride + b];
+        double m = -INFINITY;
+        int64_t n = (b + 1) * ps <= lim ? ps : lim - b * ps;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(n * H));
+        if (!s) return -1;
+        for (int h = 0; h < H; ++h) {
+          const uint16_t *q = pb->q + (row * H + h) * D;
+          for (int64_t o = 0; o < n; ++o) {
+            const uint8_t *k = pb->k_cache + ((int64_t)phys * ps + o) * D;
+            const double ks = pb->k_scale ? (double)pb->k_scale[(int64_t)phys * ps + o] : 1.0;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += oracle_dec_bf16(q[d]) * (oracle_dec_e4m3(k[d]) * ks);
+            const double v = pb->sm_scale * log2e * acc;
+            s[h * n + o] = v;
+            if (v > m) m = v;
+          }
+        }
+        double z = 0.0;
+        for (int64_t i = 0; i < n * H; ++i) z += exp2(s[i] - m);
+        free(s);
+        S[b] = m + log2(z);
+      }
+      /* selection: the last attended page first, then by descending score */
+      int32_t *sel = selected + row * pb->topk;
+      for (int i = 0; i < pb->topk; ++i) sel[i] = -1;
+      int cnt = 0;
+      if (nb > 0 && pb->topk > 0) sel[cnt++] = (int32_t)(nb - 1);
+      while (cnt < pb->topk) {
+        int64_t best = -1;
+        for (int64_t b = 0; b < nb; ++b) {
+          int taken = 0;
+          for (int i = 0; i < cnt; ++i)
+            if (sel[i] == b) taken = 1;
+          if (taken) continue;
+          if (best < 0 || S[b] > S[best]) best = b;  /* strict: equal scores keep the lower page */
+        }
+        if (best < 0) break;
+        sel[cnt++] = (int32_t)best;
+      }
+      num_selected[row] = cnt;
+    }
+  }
+  return 0;
+}

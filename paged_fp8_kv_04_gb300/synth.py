@@ -301,6 +301,76 @@ def prefill_as_decode(seed: int = 6, num_tokens: int = 2048, prefix: int = 0,
 
 
 @dataclasses.dataclass
+class IndexProblem:
+    """Inputs of the indexer's block score and top-k: index queries, the e4m3 index cache
+    (num_pages, page_size, 128) with optional per-token scales, and the decode row map."""
+    q: np.ndarray                 # bf16 bits [rows, index_heads, 128]
+    k_cache: np.ndarray           # uint8 e4m3 codes [num_pages, page_size, 128]
+    k_scale: Optional[np.ndarray]  # fp32 [num_pages, page_size] or None
+    block_table: np.ndarray       # int32 [B, stride]
+    context_lens: np.ndarray      # int32 [B]
+    cu_seqlens_q: np.ndarray      # int32 [B + 1]
+    sm_scale: float
+    topk: int
+    name: str = ""
+
+    @property
+    def num_rows(self) -> int:
+        return int(self.cu_seqlens_q[-1])
+
+
+def index_problem(seed: int, context_lens: Sequence[int], q_lens: Sequence[int],
+                  index_heads: int = 1, page_size: int = 128, topk: int = 64,
+                  per_token_scale: bool = True, hot_pages: int = 8, pool_pages=None,
+                  zero_q: bool = False, name: str = "") -> IndexProblem:
+    """Seeded indexer inputs.  Index keys are N(0, 1) quantised per token (scale amax/448)
+    or, without per-token scales, quantised at a fixed scale of 1/64; each request has
+    `hot_pages` pages whose keys lean towards its first query row, so that the selection
+    has a clear top; block tables are a random permutation of the pool."""
+    rng = np.random.default_rng(seed)
+    L = np.asarray(context_lens, dtype=np.int64)
+    ql = np.asarray(q_lens, dtype=np.int64)
+    B, D, ps, H = len(L), 128, page_size, index_heads
+    npg = (L + ps - 1) // ps
+    P = int(npg.sum()) if pool_pages is None else int(pool_pages)
+    perm = rng.permutation(P).astype(np.int32)
+    stride = max(int(npg.max()), 1)
+    bt = np.full((B, stride), -1, dtype=np.int32)
+    off = 0
+    for r in range(B):
+        bt[r, :npg[r]] = perm[off:off + npg[r]]
+        off += int(npg[r])
+    rows = int(ql.sum())
+    qf = np.zeros((rows, H, D), np.float32) if zero_q else _normal(rng, (rows, H, D))
+    x = _normal(rng, (P, ps, D))
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(ql)
+    for r in range(B):
+        if npg[r] == 0 or zero_q:
+            continue
+        hot = rng.choice(int(npg[r]), size=min(hot_pages, int(npg[r])), replace=False)
+        dirn = qf[cu[r], 0] / max(float(np.linalg.norm(qf[cu[r], 0])), 1e-6)
+        for b in hot:
+            x[bt[r, b]] += (rng.uniform(0.5, 3.0) * np.sqrt(D) * 0.25) * dirn
+    if per_token_scale:
+        codes, sc = quantize_per_token(x)
+    else:
+        codes, sc = quantize_scalar(x, 1.0 / 64.0), None
+    return IndexProblem(q=bf16_bits(qf), k_cache=codes, k_scale=sc, block_table=bt,
+                        context_lens=L.astype(np.int32), cu_seqlens_q=cu,
+                        sm_scale=1.0 / float(np.sqrt(D)), topk=topk, name=name)
+
+
+def index_decode_128k(seed: int = 8) -> IndexProblem:
+    """The sparse decode's indexer step: batch 32, context 131072 (1024 pages of 128),
+    q_len 1 for the first 16 requests and 4 for the others (80 rows), one index head,
+    per-token e4m3 index keys, top 64 pages."""
+    ql = [1] * 16 + [4] * 16
+    return index_problem(seed, [131072] * 32, ql, index_heads=1, page_size=128, topk=64,
+                         name="indexer block score + top-64, batch 32, context 131072")
+
+
+@dataclasses.dataclass
 class KvWriteCase:
     """New K/V rows (bf16 bits [T, Hkv, D]), their slots, and sentinel-filled caches."""
     k_new: np.ndarray

@@ -540,4 +540,75 @@ def pin_quantize_write_round_trip(lib):
                 assert np.all(err <= bound), "dequantised value too far from the input"
 
 
+# ------------------------------------------------ indexer block score and top-k selection
+
+def _index_brute(ip):
+    """Scores and selection by materialised fp64 torch: the keys decoded through torch's
+    float8_e4m3fn, s = sm_scale * log2(e) * q . k, a block's score the base-2 log-sum-exp of
+    its attended (head, token) scores, and the selection by Python's sort."""
+    q = torch.from_numpy(ip.q.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    kc = torch.from_numpy(ip.k_cache).view(torch.float8_e4m3fn).to(torch.float64)
+    if ip.k_scale is not None:
+        kc = kc * torch.from_numpy(ip.k_scale).to(torch.float64)[..., None]
+    ps = ip.k_cache.shape[1]
+    sel_all, n_all, S_all = [], [], []
+    for r in range(len(ip.context_lens)):
+        L = int(ip.context_lens[r])
+        r0, r1 = int(ip.cu_seqlens_q[r]), int(ip.cu_seqlens_q[r + 1])
+        ql = r1 - r0
+        for tok in range(ql):
+            lim = max(0, min(L, L - ql + tok + 1))
+            nb = (lim + ps - 1) // ps
+            S = {}
+            for b in range(nb):
+                keys = kc[int(ip.block_table[r, b])][: min(ps, lim - b * ps)]   # [n, D]
+                sc = (q[r0 + tok] @ keys.T) * ip.sm_scale / np.log(2.0)       # [H, n], log2 units
+                S[b] = float(torch.logsumexp(sc.reshape(-1) * np.log(2.0), 0) / np.log(2.0))
+            order = ([nb - 1] if nb else []) + sorted((b for b in S if b != nb - 1),
+                                                       key=lambda b: (-S[b], b))
+            sel = order[: ip.topk]
+            sel_all.append(sel + [-1] * (ip.topk - len(sel)))
+            n_all.append(len(sel))
+            S_all.append(S)
+    return np.array(sel_all, dtype=np.int32).reshape(-1, ip.topk), np.array(n_all), S_all
+
+
+def pin_index_topk_brute_force(lib):
+    """Indexer scores and selection against a materialised torch computation (two index
+    heads, per-token key scales, ragged q_len with the causal cutoff, a partial last page)."""
+    ip = synth.index_problem(31, [300, 1000, 37, 129], [1, 3, 2, 1], index_heads=2,
+                             page_size=16, topk=8)
+    sel, n, S = lib.index_topk(ip)
+    bsel, bn, bS = _index_brute(ip)
+    assert np.array_equal(n, bn), "selection counts differ"
+    assert np.array_equal(sel, bsel), "selected pages differ"
+    for row, Sr in enumerate(bS):
+        for b, v in Sr.items():
+            assert abs(S[row, b] - v) <= 1e-9 * max(1.0, abs(v)), f"score row {row} page {b}"
+        assert np.all(np.isneginf(np.delete(S[row], list(Sr.keys())))), "non-candidate scored"
+
+
+def pin_index_topk_scalar_keys(lib):
+    """The same without per-token key scales (codes read at scale 1)."""
+    ip = synth.index_problem(32, [500, 64], [2, 1], index_heads=1, page_size=32, topk=5,
+                             per_token_scale=False)
+    sel, n, _ = lib.index_topk(ip)
+    bsel, bn, _ = _index_brute(ip)
+    assert np.array_equal(sel, bsel) and np.array_equal(n, bn)
+
+
+def pin_index_topk_closed_forms(lib):
+    """q = 0: every attended (head, token) scores 0, so a page's score is log2 of its count
+    of attended pairs; the full pages tie and the selection is the last attended page, then
+    pages 0, 1, 2, ...  A page count below topk selects every page."""
+    ip = synth.index_problem(33, [16 * 10 + 5, 40], [1, 2], index_heads=3, page_size=16,
+                             topk=4, zero_q=True)
+    sel, n, S = lib.index_topk(ip)
+    assert list(sel[0]) == [10, 0, 1, 2] and n[0] == 4
+    assert S[0, 0] == np.log2(3 * 16) and S[0, 10] == np.log2(3 * 5)
+    # request 1: L 40, q_len 2 -> limits 39 and 40 -> 3 pages each
+    assert list(sel[1]) == [2, 0, 1, -1] and n[1] == 3
+    assert list(sel[2]) == [2, 0, 1, -1] and S[1, 2] == np.log2(3 * 7) and S[2, 2] == np.log2(3 * 8)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

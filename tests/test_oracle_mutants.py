@@ -48,6 +48,16 @@ MUTANTS = {
                           "const int64_t row = (page * num_kv_heads) * page_size + o;"),
     "quant_v_from_k": ("quantize_row(v_new + src,", "quantize_row(k_new + src,"),
     "quant_skips_counted": ("      ++bad;\n      continue;", "      continue;"),
+    "index_cutoff_off_by_one": ("int64_t lim = L - qlen + tok + 1;", "int64_t lim = L - qlen + tok;"),
+    "index_natural_log": ("S[b] = m + log2(z);", "S[b] = m + log(z);"),
+    "index_no_forced_page": ("if (nb > 0 && pb->topk > 0) sel[cnt++] = (int32_t)(nb - 1);", ""),
+    "index_ties_to_higher": ("if (best < 0 || S[b] > S[best]) best = b;",
+                             "if (best < 0 || S[b] >= S[best]) best = b;"),
+    "index_scale_dropped": ("(double)pb->k_scale[(int64_t)phys * ps + o] : 1.0;", "1.0 : 1.0;"),
+    "index_first_head_only": ("for (int64_t i = 0; i < n * H; ++i) z += exp2(s[i] - m);",
+                              "for (int64_t i = 0; i < n; ++i) z += exp2(s[i] - m);"),
+    "index_no_log2e": ("const double v = pb->sm_scale * log2e * acc;",
+                       "const double v = pb->sm_scale * acc;"),
 }
 
 
