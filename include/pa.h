@@ -268,6 +268,53 @@ typedef struct pa_kv_write_args {
  * launch fails. */
 pa_status_t pa_kv_quantize_write(const pa_kv_write_args_t *args, void *stream);
 
+/* ---- the indexer: block score and top-k page selection for the sparse decode ---- */
+
+#define PA_DEV_BAD_INDEX_ROW 0x200u /* pa_index_topk: q_len < 0 or > max_q_len, context_len < q_len, rows past num_rows, or more pages than the stride (the request's rows are skipped) */
+
+/* Arguments of pa_index_topk.  All pointers are device pointers. */
+typedef struct pa_index_args {
+  const void *q;                 /* bf16 [num_rows, index_heads, head_dim], 16-B aligned */
+  const void *k_cache;           /* index cache, e4m3 bytes [num_pages, page_size, head_dim], 16-B aligned */
+  const float *k_scale;          /* fp32 [num_pages, page_size], or NULL: codes read at scale 1 */
+  const int32_t *block_table;    /* [num_seqs, block_table_stride] physical page of each logical page */
+  const int32_t *context_lens;   /* [num_seqs] */
+  const int32_t *cu_seqlens_q;   /* [num_seqs + 1]: rows of request r are [cu[r], cu[r+1]) */
+  int32_t *selected;             /* out: [num_rows, topk] logical pages, -1 after num_selected */
+  int32_t *num_selected;         /* out: [num_rows] */
+  float *scores;                 /* out: [num_rows, block_table_stride] page scores (log2 units),
+                                    -inf where a page holds no attended position; 16-B aligned */
+  uint32_t *status;              /* nullable: PA_DEV_BAD_PAGE, PA_DEV_BAD_INDEX_ROW are OR-ed in */
+  int64_t num_pages;
+  int32_t num_seqs;
+  int32_t num_rows;
+  int32_t index_heads;           /* >= 1; max_q_len * index_heads <= 16 */
+  int32_t head_dim;              /* 128 */
+  int32_t page_size;             /* 16, 32, 64 or 128 */
+  int32_t topk;                  /* 1 .. 1024 */
+  int32_t block_table_stride;    /* 1 .. 16384 */
+  int32_t max_q_len;             /* bound on any request's q_len, >= 1 */
+  float sm_scale;                /* > 0 */
+  int32_t reserved;              /* 0 */
+} pa_index_args_t;
+
+/* The indexer step before the sparse decode (ROCm/ATOM PR 2122, section 1: the index
+ * cache of (num_blocks, 128, 128) e4m3 codes and the block score q . k * sm_scale * log2(e);
+ * section 2: rows map to requests through cu_seqlens_q, and row tok of a request with
+ * context L and q_len rows attends positions < L - q_len + tok + 1).  For each row:
+ *   s[h][p] = sm_scale * log2(e) * sum_d q[row][h][d] * k[p][d] * k_scale[p] over the
+ *     attended positions p, where k is the index key at p (through the block table);
+ *   scores[row][b] = log2 sum_h sum_{attended p in page b} 2^s[h][p] (-inf if none);
+ *   selected[row] = the row's last attended page, then the other candidates by descending
+ *     score (equal scores: lower page first), topk entries at most, -1 after.
+ * With q_len 1 rows are requests, and selected / num_selected are pa_decode's
+ * selected_pages / num_selected.  Inputs must be finite.  Two kernel launches on
+ * `stream`; no host synchronisation, no allocation.  PA_ERR_INVALID_ARG for a missing
+ * pointer or a value out of range, PA_ERR_ALIGN for a misaligned pointer,
+ * PA_ERR_UNSUPPORTED for head_dim, page_size or max_q_len * index_heads outside the
+ * limits above, PA_ERR_CUDA when a launch fails. */
+pa_status_t pa_index_topk(const pa_index_args_t *args, void *stream);
+
 /* ---- test hooks: exact integer / byte outputs of the row map and the page gather ---- */
 
 /* For every query row: (request, query token, causal cutoff) as int32 triples into the

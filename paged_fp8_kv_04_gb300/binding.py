@@ -76,6 +76,20 @@ class KvWriteArgs(ctypes.Structure):
 
 
 DEV_BAD_SLOT = 0x100
+DEV_BAD_INDEX_ROW = 0x200
+
+
+class IndexArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
+                ("cu_seqlens_q", ctypes.c_void_p), ("selected", ctypes.c_void_p),
+                ("num_selected", ctypes.c_void_p), ("scores", ctypes.c_void_p),
+                ("status", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
+                ("num_seqs", ctypes.c_int32), ("num_rows", ctypes.c_int32),
+                ("index_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("block_table_stride", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float), ("reserved", ctypes.c_int32)]
 
 _lib = None
 P = ctypes.c_void_p
@@ -126,6 +140,8 @@ def lib(path: Optional[str] = None):
     L.pa_decode_noalloc.restype = ctypes.c_int
     L.pa_kv_quantize_write.argtypes = [ctypes.POINTER(KvWriteArgs), P]
     L.pa_kv_quantize_write.restype = ctypes.c_int
+    L.pa_index_topk.argtypes = [ctypes.POINTER(IndexArgs), P]
+    L.pa_index_topk.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -326,3 +342,37 @@ def kv_quantize_write(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_s
     st = lib().pa_kv_quantize_write(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
     if st != 0:
         raise PaError(st, "pa_kv_quantize_write")
+
+
+def index_args(q, k_cache, k_scale, block_table, context_lens, cu_seqlens_q, selected,
+               num_selected, scores, *, topk, max_q_len, sm_scale, status=None) -> IndexArgs:
+    """pa_index_args_t over torch tensors: q bf16 [rows, heads, 128], k_cache uint8
+    [num_pages, page_size, 128], k_scale fp32 [num_pages, page_size] or None, int32 block
+    table / context lens / cu_seqlens_q, outputs selected int32 [rows, topk], num_selected
+    int32 [rows], scores fp32 [rows, stride]."""
+    a = IndexArgs()
+    a.q, a.k_cache, a.k_scale = _ptr(q), _ptr(k_cache), _ptr(k_scale)
+    a.block_table, a.context_lens, a.cu_seqlens_q = _ptr(block_table), _ptr(context_lens), _ptr(cu_seqlens_q)
+    a.selected, a.num_selected, a.scores, a.status = (_ptr(selected), _ptr(num_selected),
+                                                      _ptr(scores), _ptr(status))
+    a.num_pages = int(k_cache.shape[0])
+    a.num_seqs = int(context_lens.shape[0])
+    a.num_rows = int(q.shape[0])
+    a.index_heads = int(q.shape[1])
+    a.head_dim = int(q.shape[2])
+    a.page_size = int(k_cache.shape[1])
+    a.topk = int(topk)
+    a.block_table_stride = int(block_table.shape[1])
+    a.max_q_len = int(max_q_len)
+    a.sm_scale = float(sm_scale)
+    a.reserved = 0
+    return a
+
+
+def index_topk(args: IndexArgs, device=None, stream=None) -> None:
+    """Enqueues pa_index_topk on `stream` (default: torch's current stream)."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    st = lib().pa_index_topk(ctypes.byref(args), ctypes.c_void_p(s.cuda_stream))
+    if st != 0:
+        raise PaError(st, "pa_index_topk")

@@ -149,6 +149,19 @@ __device__ __forceinline__ void mask_scores(float (&s0)[N], float (&s1)[N],
   }
 }
 
+// The per-token V scales of the columns mask_scores masks, set to 0: an empty page slot's
+// scale in shared memory is whatever an earlier tile or kernel left there, and a masked
+// column's probability 0 times a NaN scale would still be NaN.
+template <int N>
+__device__ __forceinline__ void mask_weights(float (&w)[N], const int (&pos0)[N / 4], int cut) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int j = k >> 1, hf = j >> 1;
+    const int pos = pos0[hf] + 8 * (j & 1) + (k & 1);
+    if (pos0[hf] < 0 || pos >= cut) w[k] = 0.f;
+  }
+}
+
 // P fragments of the chunk's two PV k-steps from the probabilities (per-column scale w).
 template <int N>
 __device__ __forceinline__ void pack_p(const float (&s0)[N], const float (&s1)[N],
@@ -229,7 +242,10 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
     s1[2 * j] = acc[j][2] * c[2 * j];
     s1[2 * j + 1] = acc[j][3] * c[2 * j + 1];
   }
-  if (masked) mask_scores<NC>(s0, s1, pos0, cut);
+  if (masked) {
+    mask_scores<NC>(s0, s1, pos0, cut);
+    if (SM == PA_SCALE_PER_TOKEN) mask_weights<NC>(vw, pos0, cut);
+  }
   online_row<NC>(s0, f.m[0], f.l[0], f.o, 0);
   online_row<NC>(s1, f.m[1], f.l[1], f.o, 2);
   uint32_t pa[NKS][4];

@@ -431,6 +431,8 @@ __device__ void run_softmax(const KParams &p, const Smem &sm, const UBars &ub, i
       const int pos = pp < 0 ? -1 : pp + (t & (p.ps - 1));
       masked = pos < 0 || pos >= L;  // one query token: the cutoff is L
     }
+    // a masked slot's scales may be stale shared memory (an empty page slot), NaN included
+    if (masked) vs = 0.f;
     float alpha[8], gam[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {

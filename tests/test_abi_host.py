@@ -282,3 +282,41 @@ def test_kv_quantize_write_refusals(lib):
     assert call(k_scale=0x600002) == ALIGN
     assert call(slot_mapping=0x300004) == ALIGN
     assert call(status=0x800002) == ALIGN
+
+
+def _ix_args(**over):
+    a = B.IndexArgs()
+    vals = dict(q=0x100000, k_cache=0x200000, k_scale=0x300000, block_table=0x400000,
+                context_lens=0x500000, cu_seqlens_q=0x600000, selected=0x700000,
+                num_selected=0x800000, scores=0x900000, status=None, num_pages=64,
+                num_seqs=2, num_rows=0, index_heads=1, head_dim=128, page_size=128, topk=8,
+                block_table_stride=16, max_q_len=1, sm_scale=0.088, reserved=0)
+    vals.update(over)
+    for k, v in vals.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_index_topk_refusals(lib):
+    """pa_index_topk checks its arguments before touching a device; with no rows a valid
+    call enqueues nothing and succeeds."""
+    call = lambda **kw: lib.pa_index_topk(ctypes.byref(_ix_args(**kw)), None)
+    assert lib.pa_index_topk(None, None) == INVALID
+    assert call() == OK
+    assert call(head_dim=64) == UNSUP
+    assert call(page_size=8) == UNSUP
+    assert call(max_q_len=5, index_heads=4) == UNSUP
+    assert call(max_q_len=4, index_heads=4) == OK
+    assert call(topk=0) == INVALID
+    assert call(topk=2048) == INVALID
+    assert call(block_table_stride=0) == INVALID
+    assert call(block_table_stride=20000) == INVALID
+    assert call(sm_scale=0.0) == INVALID
+    assert call(sm_scale=float("inf")) == INVALID
+    assert call(num_seqs=0) == INVALID
+    assert call(reserved=1) == INVALID
+    assert call(scores=None) == INVALID
+    assert call(k_scale=None) == OK
+    assert call(k_cache=0x200008) == ALIGN
+    assert call(scores=0x900004) == ALIGN
+    assert call(selected=0x700002) == ALIGN

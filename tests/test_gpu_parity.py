@@ -380,3 +380,24 @@ def test_prefill_as_decode_full_size_sampled():
     """The bench's prefill workload (2048 tokens after 6144), sampled rows."""
     check_against_oracle(synth.prefill_as_decode(6, 2048, 6144), sample=[0, 1, 1023, 2047],
                          what="prefill 2K after 6K")
+
+
+@pytest.mark.parametrize("tc", [False, True])
+def test_empty_page_slots_after_nan_in_shared_memory(tc):
+    """Sparse decode whose tiles have empty page slots (3 selected pages of 16 tokens in a
+    128-token tile), launched right after a kernel that stages NaN through shared memory:
+    the empty slots' stale per-token scales must not reach the output."""
+    p = synth.make_problem(48, num_seqs=6, context_lens=[300, 77, 1000, 16, 129, 500],
+                           q_lens=[1] * 6, page_size=16, selected_pages=3)
+    d = dv.to_device(p)
+    plan = dv.plan_for(p, tcgen05=tc)
+    x = torch.full((2048, 2048), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        y = x @ x
+    out, lse = dv.run(plan, p, d, lse=True)
+    torch.cuda.synchronize()
+    del y
+    assert plan.device_status() == 0
+    ref, ref_lse = O.decode(p)
+    compare(out.float().cpu().numpy(), ref, f"empty slots after NaN smem tcgen05={tc}")
+    compare_lse(lse.cpu().numpy(), ref_lse, "lse")
