@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dense8k",
                     choices=["dense8k", "bf16ctl", "long128k_scalar", "long128k", "ragged",
-                             "sparse", "kv_write", "prefill"])
+                             "sparse", "kv_write", "prefill", "indexer"])
     ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = balanced)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -58,8 +58,8 @@ def parse():
 # (sha256 over the C header and the decode kernels' translation unit); any other source
 # gives traffic null.
 MEASURED_TRAFFIC = {
-    "dense8k": {"bytes": 69464320 + 693760,
-                "csrc_sha256": "68cd066aaee732fa5b9250ed075613948eed8cd5ca682b94808a265df79ac4aa",
+    "dense8k": {"bytes": 69465856 + 834560,
+                "csrc_sha256": "4509608146fd3b34cf49300afe4b0fb732da38b6296e1bf93510b38912d79c07",
                 "profile": "profiles/decode_kernel_dense8k_full.md"},
 }
 
@@ -351,6 +351,8 @@ def bench_ours(args):
 
     if args.workload == "kv_write":
         return bench_kv_write(args, dev, rank, world, local)
+    if args.workload == "indexer":
+        return bench_indexer(args, dev, rank, world, local)
     p, desc = make_workload(args.workload)
     d = dv.to_device(p, dev)
     plan = dv.plan_for(p, device=dev, partition_tokens=args.partition, tcgen05=args.tcgen05)
@@ -516,6 +518,102 @@ def bench_ours(args):
 
 
 KV_WRITE_METRIC = "FP8 KV quantise-and-write: achieved HBM GB/s (% of GB300 peak)"
+INDEXER_METRIC = "Indexer block score + top-k: achieved HBM GB/s (% of GB300 peak)"
+
+
+def indexer_bytes(ip):
+    """Index keys (128 B) and scales (4 B) of every position of every request, read once
+    per request; queries, page scores, selections and the block table."""
+    ps = ip.k_cache.shape[1]
+    pos = int(ip.context_lens.astype(np.int64).sum())
+    pages = int(((ip.context_lens.astype(np.int64) + ps - 1) // ps).sum())
+    per = 128 + (4 if ip.k_scale is not None else 0)
+    R, H = ip.q.shape[:2]
+    out = R * ip.block_table.shape[1] * 4 + R * ip.topk * 4 + R * 4
+    return pos * per + R * H * 128 * 2 + out + pages * 4
+
+
+def bench_indexer(args, dev, rank, world, local):
+    """pa_index_topk on the sparse decode's indexer step (batch 32, context 131072)."""
+    import torch
+    from paged_fp8_kv_04_gb300 import binding as B, synth
+    ip = synth.index_decode_128k(8)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q, kc = t(ip.q.view(np.int16)), t(ip.k_cache)
+    ks = None if ip.k_scale is None else t(ip.k_scale)
+    bt, L, cu = t(ip.block_table), t(ip.context_lens), t(ip.cu_seqlens_q)
+    R, stride = ip.num_rows, ip.block_table.shape[1]
+    sel = torch.empty((R, ip.topk), dtype=torch.int32, device=dev)
+    nsel = torch.empty((R,), dtype=torch.int32, device=dev)
+    scores = torch.empty((R, stride), dtype=torch.float32, device=dev)
+    maxq = int(np.diff(ip.cu_seqlens_q).max())
+    a = B.index_args(q, kc, ks, bt, L, cu, sel, nsel, scores, topk=ip.topk, max_q_len=maxq,
+                     sm_scale=ip.sm_scale)
+    total = indexer_bytes(ip)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3) + args.profile):
+            B.index_topk(a, stream=stream)
+    torch.cuda.synchronize(dev)
+    if args.profile:
+        print(json.dumps({"profile_calls": max(args.warmup, 3) + args.profile}), flush=True)
+        return
+    K = args.steps
+    chunk = max(c_ for c_ in range(1, min(K, 100) + 1) if K % c_ == 0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(chunk):
+            B.index_topk(a, stream=stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K // chunk):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    us = ms / K * 1e3
+    achieved = total / (us * 1e-6) / 1e9
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu:
+        from oracle import oracle as O
+        one = dataclasses.replace(ip, q=ip.q[:1], block_table=ip.block_table[:1],
+                                  context_lens=ip.context_lens[:1],
+                                  cu_seqlens_q=np.array([0, 1], dtype=np.int32))
+        t0 = time.perf_counter()
+        passes = 0
+        while time.perf_counter() - t0 < 5.0:
+            O.index_topk(one)
+            passes += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": indexer_bytes(one) * passes / dt / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"request 0 (one row, 131072 positions), {passes} times, {dt:.1f} s"}
+    peak, peak_kind = peak_hbm()
+    line = {
+        "metric": INDEXER_METRIC, "value": achieved, "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 keys, f32 dot products",
+        "data": "synthetic",
+        "config": {"workload": ip.name, "l2": "one 554 MB index cache (> 3 x L2)",
+                   "timed": "CUDA graph replay of back-to-back pa_index_topk calls (two launches each)"},
+        "us_per_call_graph": us, "rows_per_s": R / (us * 1e-6),
+        "algorithmic_bytes_per_call": int(total),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * K, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
 
 
 def kv_write_bytes(c):
