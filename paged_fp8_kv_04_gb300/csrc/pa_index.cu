@@ -2,9 +2,9 @@
 // See include/pa.h for the contract.
 //
 // Two launches.  index_score_kernel streams the e4m3 index cache once per request (a
-// warp per page, a token per lane and 16 dimensions at a time, the request's index
-// queries in shared memory as fp32) and writes each (row, page) score: the base-2
-// log-sum-exp of the page's attended (head, token) scores.  index_select_kernel, a CTA
+// warp per page; the request's index query rows against the page's tokens on the tensor
+// cores, mma.sync m16n8k16 in f16 with fp32 accumulation) and writes each (row, page)
+// score: the base-2 log-sum-exp of the page's attended (head, token) scores.  index_select_kernel, a CTA
 // per row, sorts that row's candidate pages by score in shared memory (bitonic, keys of
 // score and page index) with the row's last attended page forced first, and writes the
 // first topk.  HBM-bound on the index cache: 128 B per position per request.
@@ -14,12 +14,17 @@
 #include <cmath>
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 #include "pa.h"
+#include "pa_ptx.cuh"
 
 namespace {
 
 constexpr int kD = 128;
-constexpr int kWarps = 8;           // pages per CTA of the score kernel
+constexpr int kWarps = 8;           // warps per CTA of the score kernel
+constexpr int kPagesPerWarp = 4;    // pages each warp of the score kernel scores
+constexpr bool kPipe = false;       // double-buffered loads in the score kernel
 constexpr int kMaxRowHeads = 16;    // q_len * index_heads of one request
 constexpr int kMaxStride = 16384;   // pages per row the selection sorts
 constexpr int kMaxTopk = 1024;
@@ -37,17 +42,6 @@ struct IdxParams {
   float cscale;  // sm_scale * log2(e)
 };
 
-__device__ __forceinline__ void e4m3x2_f32(uint32_t x, float &lo, float &hi) {
-  asm("{\n\t.reg .b16 c, l, h;\n\t.reg .b32 w;\n\t"
-      "cvt.u16.u32 c, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 w, c;\n\t"
-      "mov.b32 {l, h}, w;\n\t"
-      "cvt.f32.f16 %0, l;\n\t"
-      "cvt.f32.f16 %1, h;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(x));
-}
-
 __device__ __forceinline__ uint4 load_nc16(const void *ptr) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -56,26 +50,19 @@ __device__ __forceinline__ uint4 load_nc16(const void *ptr) {
   return r;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Request blockIdx.y, pages blockIdx.x * kWarps + warp.  RH: q_len * index_heads rounded
-// up to a power of two (rows past the request's are computed and dropped).
-template <int RH>
+// Request blockIdx.y, pages blockIdx.x * kWarps + warp.  The request's q_len * heads
+// query rows (at most 16, padded with zeros) are the M = 16 rows of mma.sync m16n8k16 in
+// f16 (bf16 -> f16 is exact for 2^-14 <= |q| <= 65504); the page's tokens are the N
+// columns, 8 per n-tile; its e4m3 codes widen exactly to f16.  The reduction index is
+// permuted: in k-step kk, lane (g, t) supplies real dimensions 32 t + 4 kk + 0..3 for both
+// operands, so each lane reads 32 contiguous bytes of a token row and the four lanes of a
+// quad cover the whole 128-byte row.
 __global__ void __launch_bounds__(kWarps * 32) index_score_kernel(const IdxParams p) {
-  __shared__ float qs[RH * kD];
+  __shared__ __align__(16) uint16_t qh[16 * kD];      // f16 query rows
+  __shared__ float rowstat[kWarps][16][2];           // per warp: (max, sum) of each row
   const int r = blockIdx.y;
   const int L = p.L[r], row0 = p.cu[r], ql = p.cu[r + 1] - row0;
-  if (ql < 0 || ql > p.maxq || L < ql || (int64_t)ql * p.H > RH || row0 < 0 || row0 + ql > p.R ||
+  if (ql < 0 || ql > p.maxq || L < ql || (int64_t)ql * p.H > 16 || row0 < 0 || row0 + ql > p.R ||
       ((L + p.ps - 1) >> p.ps_shift) > p.stride) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && p.status != nullptr)
       atomicOr(p.status, PA_DEV_BAD_INDEX_ROW);
@@ -83,96 +70,159 @@ __global__ void __launch_bounds__(kWarps * 32) index_score_kernel(const IdxParam
   }
   if (ql == 0) return;
   const int npg = min((L + p.ps - 1) >> p.ps_shift, p.stride);
-  if ((int)blockIdx.x * kWarps >= npg) return;  // the same for the whole CTA
+  if ((int)blockIdx.x * kWarps * kPagesPerWarp >= npg) return;  // the same for the whole CTA
   const int nrh = ql * p.H;
-  for (int i = threadIdx.x; i < RH * kD; i += kWarps * 32)
-    qs[i] = i < nrh * kD ? __uint_as_float((uint32_t)p.q[(int64_t)row0 * p.H * kD + i] << 16) : 0.f;
+  bool qbad = false;
+  for (int i = threadIdx.x; i < 16 * kD; i += kWarps * 32) {
+    float v = 0.f;
+    if (i < nrh * kD) v = __uint_as_float((uint32_t)p.q[(int64_t)row0 * p.H * kD + i] << 16);
+    qbad |= fabsf(v) > 65504.f;
+    qh[i] = __half_as_ushort(__float2half_rn(v));
+  }
+  if (qbad && p.status != nullptr) atomicOr(p.status, PA_DEV_Q_RANGE);
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kWarps + warp;
-  if (b >= npg) return;
-  const int phys = p.bt[(int64_t)r * p.stride + b];
-  if (phys < 0 || phys >= p.num_pages) {
-    if (lane == 0 && p.status != nullptr) atomicOr(p.status, PA_DEV_BAD_PAGE);
-    for (int t = lane; t < ql; t += 32) p.scores[(int64_t)(row0 + t) * p.stride + b] = -INFINITY;
-    return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  // this warp's pages: b_i = blockIdx.x * kWarps * kPagesPerWarp + warp + kWarps * i
+  const int bfirst = blockIdx.x * kWarps * kPagesPerWarp + warp;
+  int npw = 0;
+  while (npw < kPagesPerWarp && bfirst + kWarps * npw < npg) ++npw;
+  if (npw == 0) return;
+  int my_phys = 0;  // lane i holds page i's physical page
+  if (lane < npw) my_phys = p.bt[(int64_t)r * p.stride + bfirst + kWarps * lane];
+  const bool my_bad = lane < npw && (my_phys < 0 || my_phys >= p.num_pages);
+  if (__any_sync(0xffffffffu, my_bad) && lane == 0 && p.status != nullptr)
+    atomicOr(p.status, PA_DEV_BAD_PAGE);
+  // A fragments of the 8 k-steps
+  uint32_t af[8][4];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int d = 32 * t + 4 * kk;
+    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(qh + g * kD + d);
+    const uint32_t *r8 = reinterpret_cast<const uint32_t *>(qh + (g + 8) * kD + d);
+    af[kk][0] = r0[0];
+    af[kk][1] = r8[0];
+    af[kk][2] = r0[1];
+    af[kk][3] = r8[1];
   }
-  // The lane's tokens t = lane + 32 i (i < 4, t < page_size), one at a time: a dot product
-  // per (row, head) j, then a running (max, sum of 2^(s - max)) per j over the lane's
-  // attended tokens; the warp combines them per row at the end.
-  float m[RH], z[RH];
+  // rows g and g + 8: the cutoff of their query token (padding rows attend nothing)
+  const int rowA = g, rowB = g + 8;
+  const int limA = rowA < nrh ? L - ql + rowA / p.H + 1 : INT_MIN;
+  const int limB = rowB < nrh ? L - ql + rowB / p.H + 1 : INT_MIN;
+  const int ntiles = p.ps >> 3, ngr = (ntiles + 3) >> 2, total = npw * ngr;
+
+  struct Buf {
+    uint4 raw[4][2];
+    float ks[4][2];
+  };
+  // loads of step `it`: page it / ngr, n-tiles 4 (it % ngr) .. + 3
+  auto load = [&](int it, Buf &bf) {
+    const int i = it / ngr, j0 = 4 * (it - i * ngr);
+    int ph = __shfl_sync(0xffffffffu, my_phys, i);
+    const bool bad = __shfl_sync(0xffffffffu, my_bad ? 1 : 0, i) != 0;
+    if (bad) ph = 0;  // read a valid page; the page's scores are written as -inf
+    const uint8_t *kp = p.k + (int64_t)ph * p.ps * kD + 32 * t;
 #pragma unroll
-  for (int j = 0; j < RH; ++j) {
-    m[j] = -INFINITY;
-    z[j] = 0.f;
-  }
-  const uint8_t *kp = p.k + (int64_t)phys * p.ps * kD;
-  const int pos0 = b * p.ps, lim_last = L;  // row ql-1 attends every position < L
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i) {
-    const int t = lane + 32 * i;
-    if (t >= p.ps || pos0 + t >= lim_last) continue;  // no row attends it
-    uint4 raw[kD / 16];
-#pragma unroll
-    for (int c = 0; c < kD / 16; ++c) raw[c] = load_nc16(kp + (int64_t)t * kD + c * 16);
-    float acc[RH];
-#pragma unroll
-    for (int j = 0; j < RH; ++j) acc[j] = 0.f;
-#pragma unroll
-    for (int c = 0; c < kD / 16; ++c) {
-      float kf[16];
-      const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        e4m3x2_f32(w[e] & 0xFFFFu, kf[4 * e + 0], kf[4 * e + 1]);
-        e4m3x2_f32(w[e] >> 16, kf[4 * e + 2], kf[4 * e + 3]);
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      if (j < ntiles) {
+        const uint8_t *row = kp + (int64_t)(8 * j + g) * kD;
+        bf.raw[u][0] = load_nc16(row);
+        bf.raw[u][1] = load_nc16(row + 16);
+        const int tk = 8 * j + 2 * t;
+        bf.ks[u][0] = p.ks != nullptr ? __ldg(p.ks + (int64_t)ph * p.ps + tk) : 1.f;
+        bf.ks[u][1] = p.ks != nullptr ? __ldg(p.ks + (int64_t)ph * p.ps + tk + 1) : 1.f;
       }
+    }
+  };
+  float mA = -INFINITY, zA = 0.f, mB = -INFINITY, zB = 0.f;
+  auto fold = [&](float v, int pos, int lim, float &m, float &z) {
+    if (pos >= lim) return;
+    if (v > m) {
+      z = z * exp2f(m - v) + 1.f;
+      m = v;
+    } else {
+      z += exp2f(v - m);
+    }
+  };
+  auto compute = [&](int it, const Buf &bf) {
+    const int i = it / ngr, j0 = 4 * (it - i * ngr);
+    const int pos0 = (bfirst + kWarps * i) * p.ps;
 #pragma unroll
-      for (int j = 0; j < RH; ++j) {
-        const float4 *q4 = reinterpret_cast<const float4 *>(qs + j * kD + c * 16);
-        float a = acc[j];
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      if (j >= ntiles) break;
+      const uint32_t w[8] = {bf.raw[u][0].x, bf.raw[u][0].y, bf.raw[u][0].z, bf.raw[u][0].w,
+                             bf.raw[u][1].x, bf.raw[u][1].y, bf.raw[u][1].z, bf.raw[u][1].w};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 qv = q4[e];
-          a = fmaf(qv.x, kf[4 * e + 0], a);
-          a = fmaf(qv.y, kf[4 * e + 1], a);
-          a = fmaf(qv.z, kf[4 * e + 2], a);
-          a = fmaf(qv.w, kf[4 * e + 3], a);
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1;
+        pa::e4m3x4_to_f16x2x2(w[kk], b0, b1);
+        pa::mma_f16(acc, af[kk], b0, b1);
+      }
+      const int tk = 8 * j + 2 * t;
+      const float s0 = p.cscale * bf.ks[u][0], s1 = p.cscale * bf.ks[u][1];
+      fold(acc[0] * s0, pos0 + tk, limA, mA, zA);
+      fold(acc[1] * s1, pos0 + tk + 1, limA, mA, zA);
+      fold(acc[2] * s0, pos0 + tk, limB, mB, zB);
+      fold(acc[3] * s1, pos0 + tk + 1, limB, mB, zB);
+    }
+  };
+  auto finish = [&](int i) {  // page i of the warp: combine, write, reset
+    const int bpage = bfirst + kWarps * i;
+    const bool bad = __shfl_sync(0xffffffffu, my_bad ? 1 : 0, i) != 0;
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {  // the quad's four lanes hold the same two rows
+      const float m2A = __shfl_xor_sync(0xffffffffu, mA, o), z2A = __shfl_xor_sync(0xffffffffu, zA, o);
+      const float m2B = __shfl_xor_sync(0xffffffffu, mB, o), z2B = __shfl_xor_sync(0xffffffffu, zB, o);
+      const float nA = fmaxf(mA, m2A), nB = fmaxf(mB, m2B);
+      zA = (nA == -INFINITY) ? 0.f : zA * exp2f(mA - nA) + z2A * exp2f(m2A - nA);
+      zB = (nB == -INFINITY) ? 0.f : zB * exp2f(mB - nB) + z2B * exp2f(m2B - nB);
+      mA = nA;
+      mB = nB;
+    }
+    if (t == 0) {
+      rowstat[warp][rowA][0] = mA;
+      rowstat[warp][rowA][1] = zA;
+      rowstat[warp][rowB][0] = mB;
+      rowstat[warp][rowB][1] = zB;
+    }
+    __syncwarp();
+    if (lane < ql) {  // query token `lane`: its heads' rows
+      float M = -INFINITY;
+      for (int h = 0; h < p.H; ++h) M = fmaxf(M, rowstat[warp][lane * p.H + h][0]);
+      float Z = 0.f;
+      if (M != -INFINITY)
+        for (int h = 0; h < p.H; ++h) {
+          const float mh = rowstat[warp][lane * p.H + h][0];
+          if (mh != -INFINITY) Z += rowstat[warp][lane * p.H + h][1] * exp2f(mh - M);
         }
-        acc[j] = a;
-      }
+      p.scores[(int64_t)(row0 + lane) * p.stride + bpage] =
+          (bad || M == -INFINITY) ? -INFINITY : M + log2f(Z);
     }
-    const float sc = p.cscale * (p.ks != nullptr ? p.ks[(int64_t)phys * p.ps + t] : 1.f);
-#pragma unroll
-    for (int j = 0; j < RH; ++j) {
-      if (j >= nrh) break;
-      const int tok = j / p.H;
-      if (pos0 + t >= L - ql + tok + 1) continue;  // past this row's cutoff
-      const float sv = acc[j] * sc;
-      if (sv > m[j]) {
-        z[j] = z[j] * exp2f(m[j] - sv) + 1.f;
-        m[j] = sv;
-      } else {
-        z[j] += exp2f(sv - m[j]);
-      }
+    __syncwarp();
+    mA = mB = -INFINITY;
+    zA = zB = 0.f;
+  };
+  if (kPipe) {  // two buffers, the next step's loads issued before this step's arithmetic
+    Buf b0, b1;
+    load(0, b0);
+    for (int it = 0; it < total; it += 2) {
+      if (it + 1 < total) load(it + 1, b1);
+      compute(it, b0);
+      if ((it + 1) % ngr == 0) finish(it / ngr);
+      if (it + 1 >= total) break;
+      if (it + 2 < total) load(it + 2, b0);
+      compute(it + 1, b1);
+      if ((it + 2) % ngr == 0) finish((it + 1) / ngr);
     }
-  }
-  for (int tok = 0; tok < ql; ++tok) {
-    // the row's heads on this lane, then across the warp
-    float mr = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < RH; ++j)
-      if (j / p.H == tok && j < nrh) mr = fmaxf(mr, m[j]);
-    const float M = warp_max(mr);
-    float zr = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int j = 0; j < RH; ++j)
-        if (j / p.H == tok && j < nrh && m[j] != -INFINITY) zr += z[j] * exp2f(m[j] - M);
+  } else {
+    for (int it = 0; it < total; ++it) {
+      Buf bf;
+      load(it, bf);
+      compute(it, bf);
+      if ((it + 1) % ngr == 0) finish(it / ngr);
     }
-    const float Z = warp_sum(zr);
-    if (lane == 0)
-      p.scores[(int64_t)(row0 + tok) * p.stride + b] = M == -INFINITY ? -INFINITY : M + log2f(Z);
   }
 }
 
@@ -249,12 +299,6 @@ int log2_page(int ps) {
   }
 }
 
-template <int RH>
-cudaError_t launch_scores(const IdxParams &p, int gx, cudaStream_t s) {
-  index_score_kernel<RH><<<dim3(gx, p.B), kWarps * 32, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 extern "C" pa_status_t pa_index_topk(const pa_index_args_t *a, void *stream) {
@@ -303,14 +347,9 @@ extern "C" pa_status_t pa_index_topk(const pa_index_args_t *a, void *stream) {
   p.cscale = a->sm_scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int gx = (a->block_table_stride + kWarps - 1) / kWarps;
-  const int rh = a->max_q_len * a->index_heads;
-  cudaError_t e = rh <= 1   ? launch_scores<1>(p, gx, s)
-                  : rh <= 2 ? launch_scores<2>(p, gx, s)
-                  : rh <= 4 ? launch_scores<4>(p, gx, s)
-                  : rh <= 8 ? launch_scores<8>(p, gx, s)
-                            : launch_scores<16>(p, gx, s);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  const int gx = (a->block_table_stride + kWarps * kPagesPerWarp - 1) / (kWarps * kPagesPerWarp);
+  index_score_kernel<<<dim3(gx, p.B), kWarps * 32, 0, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   int n = 1;
   while (n < a->block_table_stride) n <<= 1;
   const size_t smem = (size_t)n * sizeof(unsigned long long);
