@@ -228,6 +228,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(ms, world, dev):
+    """The slowest rank's timed region (ms): every rank gets the maximum."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rates(bytes_per_step, rows_per_step, steps, world, t_max_ms):
+    """GB/s and rows/s of the whole job: every rank's steps over the slowest rank's time
+    (replicas: each rank runs the same workload)."""
+    sec = t_max_ms / 1e3
+    return world * bytes_per_step * steps / sec / 1e9, world * rows_per_step * steps / sec
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -435,14 +453,9 @@ def bench_ours(args):
     torch.cuda.synchronize(dev)
     direct_us = e2.elapsed_time(e3) / nd * 1e3
 
-    t_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(ms, world, dev)
+    value, rows_s = whole_job_rates(total_bytes, p.num_rows, K, world, t_max)
     sec = t_max / 1e3
-    value = world * total_bytes * K / sec / 1e9
-    rows_s = world * p.num_rows * K / sec
     us_per_call = ms / K * 1e3
 
     # end to end through the C ABI: pinned host inputs -> device, decode, output -> host
