@@ -231,10 +231,12 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// A CTA per row; n (a power of two >= the row stride) keys in dynamic shared memory.
-__global__ void __launch_bounds__(256) index_select_kernel(const IdxParams p, int n) {
+// A CTA per row; n (a power of two >= the row stride) keys in dynamic shared memory,
+// sorted by a bitonic network whose every stage gives each thread one compare-exchange
+// pair (up to 1024 threads).
+__global__ void __launch_bounds__(1024) index_select_kernel(const IdxParams p, int n) {
   extern __shared__ unsigned long long keys[];
-  const int row = blockIdx.x, tid = threadIdx.x;
+  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   // the request that owns the row: the last r with cu[r] <= row
   int lo = 0, hi = p.B - 1;
   while (lo < hi) {
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(256) index_select_kernel(const IdxParams p, in
     nb = lim > 0 ? min((lim + p.ps - 1) >> p.ps_shift, p.stride) : 0;
   }
   float *srow = p.scores + (int64_t)row * p.stride;
-  for (int b = tid; b < n; b += 256) {
+  for (int b = tid; b < n; b += nt) {
     unsigned long long k = 0ull;
     if (b < nb) {
       const uint32_t idx = 0xFFFFFFFFu - (uint32_t)b;
@@ -266,22 +268,20 @@ __global__ void __launch_bounds__(256) index_select_kernel(const IdxParams p, in
   __syncthreads();
   for (int k = 2; k <= n; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < n; i += 256) {
-        const int x = i ^ j;
-        if (x > i) {
-          const unsigned long long a = keys[i], c = keys[x];
-          const bool desc = (i & k) == 0;
-          if (desc ? a < c : a > c) {
-            keys[i] = c;
-            keys[x] = a;
-          }
+      for (int q = tid; q < (n >> 1); q += nt) {
+        const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1)), x = i + j;  // i has bit j clear
+        const unsigned long long a = keys[i], c = keys[x];
+        const bool desc = (i & k) == 0;
+        if (desc ? a < c : a > c) {
+          keys[i] = c;
+          keys[x] = a;
         }
       }
       __syncthreads();
     }
   }
   const int cnt = min(nb, p.topk);
-  for (int i = tid; i < p.topk; i += 256)
+  for (int i = tid; i < p.topk; i += nt)
     p.sel[(int64_t)row * p.topk + i] =
         i < cnt ? (int32_t)(0xFFFFFFFFu - (uint32_t)(keys[i] & 0xFFFFFFFFull)) : -1;
   if (tid == 0) p.nsel[row] = cnt;
@@ -362,6 +362,7 @@ extern "C" pa_status_t pa_index_topk(const pa_index_args_t *a, void *stream) {
       opted = true;
     }
   }
-  index_select_kernel<<<a->num_rows, 256, smem, s>>>(p, n);
+  const int threads = n >= 2048 ? 1024 : (n >= 64 ? n / 2 : 32);
+  index_select_kernel<<<a->num_rows, threads, smem, s>>>(p, n);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
