@@ -24,7 +24,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kWarps = 8;           // warps per CTA of the score kernel
 constexpr int kPagesPerWarp = 4;    // pages each warp of the score kernel scores
-constexpr bool kPipe = false;       // double-buffered loads in the score kernel
+constexpr int kQRow = 144;          // halves per staged query row (72 words)
 constexpr int kMaxRowHeads = 16;    // q_len * index_heads of one request
 constexpr int kMaxStride = 16384;   // pages per row the selection sorts
 constexpr int kMaxTopk = 1024;
@@ -57,8 +57,10 @@ __device__ __forceinline__ uint4 load_nc16(const void *ptr) {
 // permuted: in k-step kk, lane (g, t) supplies real dimensions 32 t + 4 kk + 0..3 for both
 // operands, so each lane reads 32 contiguous bytes of a token row and the four lanes of a
 // quad cover the whole 128-byte row.
-__global__ void __launch_bounds__(kWarps * 32) index_score_kernel(const IdxParams p) {
-  __shared__ __align__(16) uint16_t qh[16 * kD];      // f16 query rows
+__global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxParams p) {
+  // f16 query rows in k-step order: row, k-step kk, lane column t, then the 4 dimensions
+  // 32 t + 4 kk + 0..3; rows 72 words apart so that a fragment load has no bank conflict
+  __shared__ __align__(16) uint16_t qh[16 * kQRow];
   __shared__ float rowstat[kWarps][16][2];           // per warp: (max, sum) of each row
   const int r = blockIdx.y;
   const int L = p.L[r], row0 = p.cu[r], ql = p.cu[r + 1] - row0;
@@ -77,7 +79,8 @@ __global__ void __launch_bounds__(kWarps * 32) index_score_kernel(const IdxParam
     float v = 0.f;
     if (i < nrh * kD) v = __uint_as_float((uint32_t)p.q[(int64_t)row0 * p.H * kD + i] << 16);
     qbad |= fabsf(v) > 65504.f;
-    qh[i] = __half_as_ushort(__float2half_rn(v));
+    const int row = i / kD, d = i - row * kD;
+    qh[row * kQRow + ((d & 31) >> 2) * 16 + (d >> 5) * 4 + (d & 3)] = __half_as_ushort(__float2half_rn(v));
   }
   if (qbad && p.status != nullptr) atomicOr(p.status, PA_DEV_Q_RANGE);
   __syncthreads();
@@ -92,17 +95,17 @@ __global__ void __launch_bounds__(kWarps * 32) index_score_kernel(const IdxParam
   const bool my_bad = lane < npw && (my_phys < 0 || my_phys >= p.num_pages);
   if (__any_sync(0xffffffffu, my_bad) && lane == 0 && p.status != nullptr)
     atomicOr(p.status, PA_DEV_BAD_PAGE);
-  // A fragments of the 8 k-steps
-  uint32_t af[8][4];
+  // A fragments of k-step kk: rows g and g + 8 at dimensions 32 t + 4 kk + 0..3
+  const uint16_t *qa = qh + g * kQRow + 4 * t, *qb = qh + (g + 8) * kQRow + 4 * t;
+  uint32_t af[8][4];  // held for the warp's pages (reading them per k-step measured slower)
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const int d = 32 * t + 4 * kk;
-    const uint32_t *r0 = reinterpret_cast<const uint32_t *>(qh + g * kD + d);
-    const uint32_t *r8 = reinterpret_cast<const uint32_t *>(qh + (g + 8) * kD + d);
-    af[kk][0] = r0[0];
-    af[kk][1] = r8[0];
-    af[kk][2] = r0[1];
-    af[kk][3] = r8[1];
+    const uint2 x = *reinterpret_cast<const uint2 *>(qa + 16 * kk);
+    const uint2 y = *reinterpret_cast<const uint2 *>(qb + 16 * kk);
+    af[kk][0] = x.x;
+    af[kk][1] = y.x;
+    af[kk][2] = x.y;
+    af[kk][3] = y.y;
   }
   // rows g and g + 8: the cutoff of their query token (padding rows attend nothing)
   const int rowA = g, rowB = g + 8;
@@ -204,25 +207,12 @@ __global__ void __launch_bounds__(kWarps * 32) index_score_kernel(const IdxParam
     mA = mB = -INFINITY;
     zA = zB = 0.f;
   };
-  if (kPipe) {  // two buffers, the next step's loads issued before this step's arithmetic
-    Buf b0, b1;
-    load(0, b0);
-    for (int it = 0; it < total; it += 2) {
-      if (it + 1 < total) load(it + 1, b1);
-      compute(it, b0);
-      if ((it + 1) % ngr == 0) finish(it / ngr);
-      if (it + 1 >= total) break;
-      if (it + 2 < total) load(it + 2, b0);
-      compute(it + 1, b1);
-      if ((it + 2) % ngr == 0) finish((it + 1) / ngr);
-    }
-  } else {
-    for (int it = 0; it < total; ++it) {
-      Buf bf;
-      load(it, bf);
-      compute(it, bf);
-      if ((it + 1) % ngr == 0) finish(it / ngr);
-    }
+  // (double-buffering the loads measured slower: the registers cost a CTA per SM)
+  for (int it = 0; it < total; ++it) {
+    Buf bf;
+    load(it, bf);
+    compute(it, bf);
+    if ((it + 1) % ngr == 0) finish(it / ngr);
   }
 }
 
