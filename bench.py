@@ -82,8 +82,8 @@ def csrc_sha256():
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
 # Its DRAM writes at kernel end are below the bytes it writes: L2 still holds dirty lines
 # when the launch ends, and writes them back during the next one.
-MEASURED_TRAFFIC_KV_WRITE = {"bytes": 136345856 + 35392512,
-                             "src_sha256": "44b6bc93ea801a2fdccab4b373d71575d565ad97b1cc5c1577eff57bf0eabaa2",
+MEASURED_TRAFFIC_KV_WRITE = {"bytes": 136342272 + 34774016,
+                             "src_sha256": "817a0d7497290567ac5cf720d6c3e352e9b49043cdd3241376c89f0623e65d20",
                              "profile": "profiles/kv_quantize_write_prefill8k_full.md"}
 
 
