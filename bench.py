@@ -55,13 +55,24 @@ def parse():
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the decode kernel
 # from one ncu capture per workload, valid only for the kernel sources they were taken on
-# (sha256 over the C header and the decode kernels' translation unit); any other source
-# gives traffic null.
+# (sha256 over the code, comments stripped, of the C header and the decode kernels'
+# translation unit); any other code gives traffic null.
 MEASURED_TRAFFIC = {
     "dense8k": {"bytes": 69465856 + 834560,
-                "csrc_sha256": "4509608146fd3b34cf49300afe4b0fb732da38b6296e1bf93510b38912d79c07",
+                "csrc_sha256": "995ba04dddd5a858e2ea922bf4682a0b2d3fdfd9723407062d3d61a762ac45d1",
                 "profile": "profiles/decode_kernel_dense8k_full.md"},
 }
+
+
+def _code_text(path):
+    """A source file without its comments and blank space, so that a comment edit keeps
+    the hash of the code it was measured on."""
+    import re
+    with open(path, "r", encoding="utf-8") as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split()).encode()
 
 
 def csrc_sha256():
@@ -74,8 +85,7 @@ def csrc_sha256():
               if f.endswith(".cuh") or f == "pa_api.cu"]
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        h.update(_code_text(f))
     return h.hexdigest()
 
 
@@ -83,7 +93,7 @@ def csrc_sha256():
 # Its DRAM writes at kernel end are below the bytes it writes: L2 still holds dirty lines
 # when the launch ends, and writes them back during the next one.
 MEASURED_TRAFFIC_KV_WRITE = {"bytes": 136342272 + 34774016,
-                             "src_sha256": "817a0d7497290567ac5cf720d6c3e352e9b49043cdd3241376c89f0623e65d20",
+                             "src_sha256": "14ed1374fc2efcd4857c515ed043605f2b2a7e636b3e29abeaa2fb2fa2330c12",
                              "profile": "profiles/kv_quantize_write_prefill8k_full.md"}
 
 
@@ -93,8 +103,7 @@ def kv_write_sha256():
     for f in (os.path.join(ROOT, "include", "pa.h"),
               os.path.join(ROOT, "paged_fp8_kv_04_gb300", "csrc", "pa_kv_write.cu")):
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        h.update(_code_text(f))
     return h.hexdigest()
 
 

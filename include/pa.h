@@ -2,7 +2,10 @@
  * pa.h -- C ABI of libpagedfp8: paged decode attention over an FP8 (e4m3) KV cache
  * with per-token or scalar K/V scales (and a BF16-KV control), for grouped-query
  * attention with ragged speculative-decode query lengths, split-K over long contexts
- * with a log-sum-exp merge, and a sparse selected-page variant.  sm_103a (GB300).
+ * with a log-sum-exp merge, and a sparse selected-page variant; with the two steps next
+ * to it: the per-token FP8 quantise-and-write that fills the cache
+ * (pa_kv_quantize_write) and the indexer's page scores and top-k that choose the sparse
+ * variant's pages (pa_index_topk).  sm_103a (GB300).
  *
  * Sources of the operation (the pages are pull-request threads):
  *  - ROCm/ATOM PR 2614, "Change": dense max-q-len-1 per-token FP8 decode and sparse
