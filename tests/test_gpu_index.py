@@ -138,3 +138,20 @@ def test_selection_feeds_sparse_decode():
     assert plan.device_status() == 0
     ref, _ = O.decode(q)
     compare(out.float().cpu().numpy(), ref, "indexer -> sparse decode")
+
+
+def test_index_degenerate_rows():
+    """A request without rows between others (equal cu_seqlens_q entries), a context
+    shorter than one page, and a single-page request whose only candidate is forced."""
+    ip = synth.index_problem(49, [300, 5, 77, 16], [2, 1, 1, 1], page_size=16, topk=4)
+    ql = [2, 0, 1, 1, 1]
+    L = np.array([300, 40, 5, 77, 16], dtype=np.int32)
+    cu = np.zeros(6, dtype=np.int32)
+    cu[1:] = np.cumsum(ql)
+    bt = np.full((5, ip.block_table.shape[1]), -1, dtype=np.int32)
+    bt[[0, 2, 3, 4]] = ip.block_table
+    bt[1, :3] = ip.block_table[0, :3]
+    ip = dataclasses.replace(ip, block_table=bt, context_lens=L, cu_seqlens_q=cu)
+    check(ip, what="degenerate rows")
+    sel, n, _ = O.index_topk(ip)
+    assert list(n) == [4, 4, 1, 4, 1]

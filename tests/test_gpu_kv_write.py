@@ -123,3 +123,12 @@ def test_producer_to_consumer_round_trip(base):
     ref, ref_lse = O.decode(q_ora)
     compare(out.float().cpu().numpy(), ref, f"round trip {base}")
     compare_lse(lse.cpu().numpy(), ref_lse, f"round trip {base}")
+
+
+def test_every_token_skipped_changes_nothing():
+    c = synth.kv_write_case(8, 50, 2, 16, 8, skip=50)
+    gk, gv, gks, gvs, status = run_gpu(c)
+    assert status == 0
+    assert np.array_equal(gk, c.k_cache) and np.array_equal(gv, c.v_cache)
+    assert np.array_equal(gks.view(np.uint32), c.k_scale.view(np.uint32))
+    assert np.array_equal(gvs.view(np.uint32), c.v_scale.view(np.uint32))
