@@ -491,7 +491,6 @@ __device__ void merge_partials(const KParams &p, int h, int row0, int qlen, int 
   for (int ub = (ctid & 255); ub < units; ub += 512) {
     const int u1 = ub + 256;  // same m-tile, same lane, accumulator index + 8
     const int mt = ub >> 9, ln = ub & 31, gg = ln >> 2, tt = ln & 3;
-    const int r0w = mt * kG + gg;
     float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
     float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
     for (int k0 = 0; k0 < n; k0 += kMergeBatch) {
