@@ -320,3 +320,20 @@ def test_index_topk_refusals(lib):
     assert call(k_cache=0x200008) == ALIGN
     assert call(scores=0x900004) == ALIGN
     assert call(selected=0x700002) == ALIGN
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built CUDA library the binding raises; there is no CPU fallback."""
+    with pytest.raises(ImportError):
+        B.lib(str(tmp_path / "libpagedfp8.so"))
+
+
+def test_product_modules_do_not_import_the_oracle():
+    """The package (binding, device helpers, input generators, build) never imports the
+    oracle: only tests, the smoke check and the benchmark's baseline legs may."""
+    import pathlib
+    import re
+    pkg = pathlib.Path(B.__file__).parent
+    for f in pkg.glob("*.py"):
+        text = f.read_text()
+        assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f"{f.name} imports the oracle"
