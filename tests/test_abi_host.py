@@ -337,3 +337,17 @@ def test_product_modules_do_not_import_the_oracle():
     for f in pkg.glob("*.py"):
         text = f.read_text()
         assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f"{f.name} imports the oracle"
+
+
+def test_oracle_and_cuda_sources_share_nothing():
+    """The C oracle includes no project header and the CUDA sources include nothing from
+    the oracle: the two sides are written independently."""
+    import pathlib
+    import re
+    root = pathlib.Path(B.__file__).parent.parent
+    oracle_src = (root / "oracle" / "pa_oracle.c").read_text()
+    incs = re.findall(r'#include\s+[<"]([^>"]+)[>"]', oracle_src)
+    assert all(i in ("math.h", "pthread.h", "stdint.h", "stdlib.h", "string.h") for i in incs), incs
+    for f in (root / "paged_fp8_kv_04_gb300" / "csrc").iterdir():
+        text = f.read_text()
+        assert "oracle" not in " ".join(re.findall(r'#include\s+[<"]([^>"]+)[>"]', text)), f.name
