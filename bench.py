@@ -307,12 +307,41 @@ def bench_reference_kv_write(args):
     print(json.dumps(line), flush=True)
 
 
+def bench_reference_indexer(args):
+    from oracle import oracle as O
+    from paged_fp8_kv_04_gb300 import synth
+    ip = synth.index_decode_128k(8)
+    one = dataclasses.replace(ip, q=ip.q[:1], block_table=ip.block_table[:1],
+                              context_lens=ip.context_lens[:1],
+                              cu_seqlens_q=np.array([0, 1], dtype=np.int32))
+    for _ in range(args.warmup):
+        O.index_topk(one)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.index_topk(one)
+    dt = time.perf_counter() - t0
+    value = indexer_bytes(one) * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": INDEXER_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": ip.name, "sample": "request 0 (one row, 131072 positions) per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "request 0 of the workload (one row)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def bench_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
     if args.workload == "kv_write":
         return bench_reference_kv_write(args)
+    if args.workload == "indexer":
+        return bench_reference_indexer(args)
     p, desc = make_workload(args.workload)
     cores = os.cpu_count() or 1
     # Each step: `cores` requests of the workload, each truncated to n leading tokens, so
