@@ -315,6 +315,22 @@ def pin_invariant_sparse_all_pages_is_dense(lib):
     _close(lib.decode(ps)[1], lib.decode(p)[1], tol=1e-13, what="lse")
 
 
+def pin_invariant_prefill_as_decode_is_one_ragged_request(lib):
+    """A prefill chunk run as one q_len-1 request per token (contexts prefix + t + 1, the
+    sequence's block table shared) equals the same chunk as one request with q_len T and
+    context prefix + T, row by row: the cutoff L - q_len + tok + 1 gives each row the
+    same keys (ROCm/ATOM PR 2614, per-token-as-decode prefill on the decode contract)."""
+    pa = synth.prefill_as_decode(51, 40, 30, page_size=16)
+    T = pa.num_seqs
+    pb = _mutate(pa, num_seqs=1, block_table=pa.block_table[:1],
+                 context_lens=np.array([30 + T], dtype=np.int32),
+                 cu_seqlens_q=np.array([0, T], dtype=np.int32), uniform_q_len=None)
+    oa, la = lib.decode(pa, threads=2)
+    ob, lb = lib.decode(pb, threads=2)
+    _close(oa, ob, what="prefill rows vs one ragged request")
+    _close(la, lb, what="lse")
+
+
 def pin_invariant_scalar_is_uniform_per_token(lib):
     p = _small(24, scale_mode="scalar")
     ks = np.full((p.num_pages, 1, p.page_size), np.float32(p.k_scale_scalar), dtype=np.float32)
