@@ -66,7 +66,7 @@ struct KParams {
   CUtensorMap tm_k;               // 2-D map over [num_pages * Hkv * page_size rows, row bytes]
   CUtensorMap tm_v;
   const uint16_t *q;
-  const uint8_t *k_cache, *v_cache;  // for L2 prefetch of upcoming pages
+  const uint8_t *k_cache, *v_cache;  // for the L2 prefetch of the first pages (before the wait)
   const float *k_scale, *v_scale;
   const int32_t *block_table, *context_lens, *cu_q, *sel, *nsel;
   void *out;
