@@ -294,14 +294,18 @@ int64_t oracle_key_positions(const oracle_problem *pb, int r, int tok, int64_t *
  * For every new token t whose slot s = slot_mapping[t] is >= 0 and every KV head h:
  *   page = s / page_size, o = s % page_size, row = (page * Hkv + h) * page_size + o;
  *   x = the token's head_dim values (bf16, read exactly);
- *   amax = max |x| and scale = amax / 448 (448: largest finite e4m3fn value), in fp32;
- *   code[d] = e4m3 of x[d] / scale, taken as the fp32 product x[d] * (448 / amax) with
- *   the reciprocal rounded to fp32 once per row (the fp32 quotient x[d] / scale where
- *   that reciprocal overflows), rounded to nearest, ties to an even mantissa, and
- *   saturated to +-448; all zero when amax = 0;
+ *   amax = max |x| and scale = amax / 448 (448: largest finite e4m3fn value), rounded
+ *   once to fp32: the scale that is stored, and the one the decode multiplies by;
+ *   code[d] = the e4m3fn value nearest to the exact real quotient x[d] / scale (ties to
+ *   an even mantissa), saturated to +-448; all zero when scale is 0;
  *   k_scale[row] = scale, k_cache[row * D + d] = code[d] (V the same).
- * The fp32 steps are the decisions a code depends on, so they are taken in fp32 here
- * as in the kernel; the rounding to e4m3 is exact arithmetic on that fp32 quotient.
+ * The quotient is taken in double: x (8 significant bits) and scale (24) are exact
+ * there, and a quotient that is not exactly an e4m3 rounding midpoint lies at least
+ * 2^-29 (relative) away from it, far beyond the 2^-53 rounding of the double division,
+ * so the double quotient falls on the same side of every midpoint as the real one, and
+ * on the midpoint itself exactly when the real one does.  (An fp32 product with
+ * 448 / amax, or an fp32 quotient rounded before the e4m3 rounding, can differ from it
+ * where x / scale is within an fp32 ulp of a midpoint.)
  * Slots >= num_pages * page_size are skipped and counted in the return value.
  * ------------------------------------------------------------------------------------ */
 
@@ -320,7 +324,7 @@ uint8_t oracle_enc_e4m3(double x) {
   int e;
   (void)frexp(a, &e);  /* a = f * 2^e, f in [0.5, 1) -> a in [2^(e-1), 2^e) */
   int ex = e - 1;      /* unbiased exponent, -6 .. 8 */
-  double m = nearbyint((ldexp(a, -ex) - 1.0) * 8.0);  /* exact: a has 24 significant bits */
+  double m = nearbyint((ldexp(a, -ex) - 1.0) * 8.0);  /* the shift and the -1 are exact */
   if (m == 8.0) {
     m = 0.0;
     ++ex;
@@ -344,16 +348,13 @@ static void quantize_row(const uint16_t *x, int D, uint8_t *code, float *scale) 
   }
   volatile float s = amax / 448.0f;  /* one fp32 division, stored as fp32 */
   *scale = s;
-  /* the division by the scale, as a product with the fp32 reciprocal 448 / amax (the
-     quotient itself where that reciprocal overflows, amax below about 1.3e-36) */
-  volatile float inv = 448.0f / amax;
   for (int d = 0; d < D; ++d) {
-    if (amax == 0.0f) {
+    if (s == 0.0f) {  /* amax = 0 (or amax / 448 below the fp32 range): nothing to encode */
       code[d] = 0;
       continue;
     }
-    volatile float q = isinf(inv) ? bf16_to_f32(x[d]) / s : bf16_to_f32(x[d]) * inv;
-    code[d] = oracle_enc_e4m3((double)q);  /* the fp32 value that decides the code */
+    const double q = (double)bf16_to_f32(x[d]) / (double)s;  /* the real quotient's side */
+    code[d] = oracle_enc_e4m3(q);
   }
 }
 

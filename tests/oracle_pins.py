@@ -376,6 +376,27 @@ def pin_golden_ragged_4_4_6_2(lib):
     assert any((r, t) != d for (_, r, t, _), d in zip(rows, div))
 
 
+def pin_golden_row_map(lib):
+    """oracle.row_map (the reference of the device row-map test) against the fixture's
+    hand-written (request, tok, cutoff) rows of the page's [4, 4, 6, 2] batch, and, on a
+    seeded ragged batch with an empty request, every row's cutoff against the length of
+    the key set the C oracle attends for that row."""
+    from oracle import oracle as O
+    meta, rows = _golden_rowmap()
+    ql, L = np.array(meta["q_lens"]), np.array(meta["context_lens"])
+    cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    rm = O.row_map(cu, L)
+    assert np.array_equal(rm, rows[:, 1:]), "row map differs from the fixture"
+    assert np.array_equal(np.arange(len(rows)), rows[:, 0])
+    ql2 = [3, 0, 1, 5, 2]
+    p = _small(28, num_seqs=5, context_lens=[9, 4, 40, 17, 2], q_lens=ql2)
+    rm2 = O.row_map(p.cu_seqlens_q, p.context_lens)
+    assert rm2.shape == (sum(ql2), 3)
+    for row, (r, tok, cut) in enumerate(rm2):
+        assert p.cu_seqlens_q[r] <= row < p.cu_seqlens_q[r + 1] and row - p.cu_seqlens_q[r] == tok
+        assert cut == lib.key_positions(p, int(r), int(tok)).size, (row, r, tok, cut)
+
+
 def pin_golden_121_rows(lib):
     """30 requests with q_len 4 plus one with q_len 1 give 121 rows (121 = 30*4 + 1);
     each row's key set ends at its own cutoff."""
@@ -554,6 +575,103 @@ def pin_quantize_write_round_trip(lib):
                 err = np.abs(y - x)
                 bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * scale) * (1 + 1e-6)
                 assert np.all(err <= bound), "dequantised value too far from the input"
+
+
+def _nearest_code_exact(q, neg):
+    """Nearest finite e4m3fn code to the non-negative rational q (a Fraction), with the
+    sign bit `neg`, by exact comparison against all 127 non-negative finite codes; ties
+    go to the even code, and q above 448 saturates to 448."""
+    from fractions import Fraction
+    codes, vals = _finite_code_values()
+    sgn = 0x80 if neg else 0x00
+    if q > 448:
+        return 0x7E | sgn
+    best, cand = None, []
+    for c, v in zip(codes, vals):
+        if c & 0x80:
+            continue
+        d = abs(Fraction(float(v)) - q)
+        if best is None or d < best:
+            best, cand = d, [int(c)]
+        elif d == best:
+            cand.append(int(c))
+    even = [c for c in cand if (c & 1) == 0]
+    return (even[0] if even else cand[0]) | sgn
+
+
+def _near_tie_rows():
+    """(amax, x) pairs of bf16 values, x <= amax, for which 448 x / amax is exactly an
+    e4m3 rounding midpoint.  With the stored scale s = fl32(amax / 448) the quotient x / s
+    is then a hair above or below that midpoint (as s was rounded up or down), so the
+    code is decided by s's rounding error: exactly where the fp32 product
+    x * fl32(448 / amax) and the fp32 quotient fl32(x / s) can land on the midpoint, or
+    on its other side, and pick the other neighbour."""
+    from fractions import Fraction
+    _, vals = _finite_code_values()
+    pos = sorted({Fraction(float(v)) for v in vals if 0 < v <= 448})
+    mids = [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]
+    out = []
+    for A in range(128, 256):                       # amax mantissas (exponent 0: amax in [1, 2))
+        amax = Fraction(A, 128)
+        for m in mids:
+            x = m * amax / 448
+            num, den = x.numerator, x.denominator
+            if den & (den - 1) or num.bit_length() > 8 or x > amax:
+                continue                            # not a bf16 value below amax
+            out.append((amax, x))
+    return out
+
+
+def pin_quantize_write_exact_quotient(lib):
+    """Each code is the e4m3 rounding of the exact real quotient x / scale, with scale the
+    stored fp32 amax / 448 (the recipe scale = amax / 448), checked with exact rational
+    arithmetic on rows built so that x / scale sits next to a rounding midpoint.  The
+    cases must include some where the fp32 product with 448 / amax and the fp32 quotient
+    each pick the other code, so that both shortcuts are told apart from the reading."""
+    from fractions import Fraction
+    pairs = _near_tie_rows()
+    assert len(pairs) >= 64, "too few near-tie rows"
+    D, ps = 128, 16
+    # one row per amax: its pairs' x values, and amax itself as the row's maximum
+    rows = {}
+    for i, (amax, x) in enumerate(pairs):
+        rows.setdefault(amax, []).append((i, x))
+    xs = np.zeros((len(rows), 1, D), dtype=np.float32)
+    meta = []
+    for t, (amax, items) in enumerate(sorted(rows.items())):
+        items = items[:D - 1]
+        for d, (i, x) in enumerate(items):
+            xs[t, 0, d] = float(x) * (-1.0 if i % 3 == 1 else 1.0)
+        xs[t, 0, D - 1] = float(amax)
+        meta.append(amax)
+    T = xs.shape[0]
+    k = synth.bf16_bits(xs)
+    assert np.array_equal(_bf16_of(k).astype(np.float64), xs.astype(np.float64)), "not bf16-exact"
+    v = k.copy()
+    P = (T + ps - 1) // ps
+    kc = np.zeros((P, 1, ps, D), np.uint8)
+    vc, ks, vs = kc.copy(), np.zeros((P, 1, ps), np.float32), np.zeros((P, 1, ps), np.float32)
+    slots = np.arange(T, dtype=np.int64)
+    lib.kv_quantize_write(k, v, slots, kc, vc, ks, vs)
+    prod_differs = quot32_differs = 0
+    for t in range(T):
+        pg, o = divmod(t, ps)
+        x = xs[t, 0].astype(np.float64)
+        s32 = np.float32(np.float32(meta[t]) / np.float32(448.0))
+        assert ks[pg, 0, o] == s32, "stored scale is not fl32(amax / 448)"
+        S = Fraction(float(s32))
+        inv32 = np.float32(np.float32(448.0) / np.float32(meta[t]))
+        for d in range(D):
+            if x[d] == 0.0:
+                continue
+            want = _nearest_code_exact(abs(Fraction(float(x[d])) / S), x[d] < 0)
+            got = int(kc[pg, 0, o, d])
+            assert got == want, f"row {t} d {d}: code {got:#x}, exact quotient gives {want:#x}"
+            prod = float(np.float32(np.float32(x[d]) * inv32))
+            quot = float(np.float32(np.float32(x[d]) / s32))
+            prod_differs += _nearest_code_exact(abs(Fraction(prod)), prod < 0) != want
+            quot32_differs += _nearest_code_exact(abs(Fraction(quot)), quot < 0) != want
+    assert prod_differs > 0 and quot32_differs > 0, (prod_differs, quot32_differs)
 
 
 # ------------------------------------------------ indexer block score and top-k selection

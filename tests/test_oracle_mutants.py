@@ -41,7 +41,13 @@ MUTANTS = {
                            "double m = nearbyint(ldexp(a, 8));"),
     "enc_no_saturation": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 480.0) return sign | 0x7F;"),
     "quant_scale_447": ("volatile float s = amax / 448.0f;", "volatile float s = amax / 447.0f;"),
-    "quant_inv_447": ("volatile float inv = 448.0f / amax;", "volatile float inv = 447.0f / amax;"),
+    "quant_fp32_product": ("const double q = (double)bf16_to_f32(x[d]) / (double)s;",
+                           "volatile float inv_m = 448.0f / amax;\n"
+                           "    volatile float q_m = bf16_to_f32(x[d]) * inv_m;\n"
+                           "    const double q = q_m;"),
+    "quant_fp32_quotient": ("const double q = (double)bf16_to_f32(x[d]) / (double)s;",
+                            "volatile float q_m = bf16_to_f32(x[d]) / s;\n"
+                            "    const double q = q_m;"),
     "quant_slot_offset": ("const int64_t page = s / page_size, o = s % page_size;",
                           "const int64_t page = s / page_size, o = (s + 1) % page_size;"),
     "quant_head_stride": ("const int64_t row = (page * num_kv_heads + h) * page_size + o;",
