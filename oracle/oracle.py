@@ -87,6 +87,10 @@ class OracleLib:
                                                  ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
                                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_kv_quantize_write.restype = ctypes.c_int64
+        lib.oracle_lse_merge.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                         ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
+                                         ctypes.c_void_p]
+        lib.oracle_lse_merge.restype = None
         lib.oracle_index_topk.argtypes = [ctypes.POINTER(_IndexProblem), ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
         lib.oracle_index_topk.restype = ctypes.c_int
@@ -158,6 +162,21 @@ class OracleLib:
         if rc != 0:
             raise RuntimeError("oracle_index_topk failed")
         return sel[:, :ip.topk], nsel, scores
+
+    def lse_merge(self, part_out, part_lse):
+        """fp64 log-sum-exp merge of partials: part_out [P, rows, heads, D], part_lse
+        [P, rows, heads] (natural log, -inf for an empty part) -> (out [rows, heads, D],
+        lse [rows, heads])."""
+        po = np.ascontiguousarray(part_out, dtype=np.float64)
+        pl = np.ascontiguousarray(part_lse, dtype=np.float64)
+        P, D = po.shape[0], po.shape[-1]
+        nv = int(np.prod(po.shape[1:-1]))
+        assert pl.shape == po.shape[:-1]
+        out = np.zeros(po.shape[1:], dtype=np.float64)
+        lse = np.zeros(pl.shape[1:], dtype=np.float64)
+        self.lib.oracle_lse_merge(po.ctypes.data, pl.ctypes.data, int(P), nv, int(D),
+                                  out.ctypes.data, lse.ctypes.data)
+        return out, lse
 
     def kv_quantize_write(self, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
         """Per-token e4m3 quantisation of new K/V rows (bf16 bit patterns [T, Hkv, D]) into
@@ -263,6 +282,10 @@ def index_topk(ip):
 def kv_quantize_write(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale):
     return default().kv_quantize_write(k_new, v_new, slot_mapping, k_cache, v_cache,
                                        k_scale, v_scale)
+
+
+def lse_merge(part_out, part_lse):
+    return default().lse_merge(part_out, part_lse)
 
 
 def row_map(cu_seqlens_q, context_lens):

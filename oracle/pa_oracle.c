@@ -472,3 +472,46 @@ int oracle_index_topk(const oracle_index_problem *pb, int32_t *selected, int32_t
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Log-sum-exp merge of attention partials: the combine step of a context split across
+ * GPUs, where each GPU attends a disjoint part of a request's positions and the parts'
+ * (normalised output, lse) are gathered and merged (the partition scratch of ROCm/ATOM
+ * PR 2710, "Smaller": max logits, exp sums and partial outputs per partition, merged into
+ * one output; one step further out, across GPUs).
+ *
+ * For every (row, head) v, over the parts i = 0 .. num_parts - 1 with lse_i > -inf:
+ *   M = max_i lse_i,  w_i = exp(lse_i - M),
+ *   out[v][d] = sum_i w_i * o_i[v][d] / sum_i w_i,   lse[v] = M + log(sum_i w_i).
+ * With every lse_i = -inf (no part attended anything): out = 0 and lse = -inf.
+ * Attention over a union of disjoint key sets is exactly this merge of the parts'
+ * attentions, since lse_i = log sum_{p in part i} exp(s_p) and o_i is the part's
+ * exp(s_p - lse_i)-weighted mean of V.
+ * ------------------------------------------------------------------------------------ */
+void oracle_lse_merge(const double *part_out, const double *part_lse, int32_t num_parts,
+                      int64_t num_vecs, int32_t dim, double *out, double *lse) {
+  for (int64_t v = 0; v < num_vecs; ++v) {
+    double M = -INFINITY;
+    for (int32_t i = 0; i < num_parts; ++i) {
+      const double l = part_lse[(int64_t)i * num_vecs + v];
+      if (l > M) M = l;
+    }
+    double *o = out + v * dim;
+    for (int32_t d = 0; d < dim; ++d) o[d] = 0.0;
+    if (M == -INFINITY) {
+      lse[v] = -INFINITY;
+      continue;
+    }
+    double z = 0.0;
+    for (int32_t i = 0; i < num_parts; ++i) {
+      const double l = part_lse[(int64_t)i * num_vecs + v];
+      if (l == -INFINITY) continue;
+      const double w = exp(l - M);
+      z += w;
+      const double *oi = part_out + ((int64_t)i * num_vecs + v) * dim;
+      for (int32_t d = 0; d < dim; ++d) o[d] += w * oi[d];
+    }
+    for (int32_t d = 0; d < dim; ++d) o[d] /= z;
+    lse[v] = M + log(z);
+  }
+}

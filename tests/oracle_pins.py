@@ -425,6 +425,73 @@ def pin_golden_q_shape_225280(lib):
     assert o.shape == (110, 16, 128)
 
 
+# ------------------------------------------------ log-sum-exp merge of a split context
+
+def _split_parts(p, nparts, rng):
+    """Each request's logical pages cut into nparts contiguous blocks (some may be empty):
+    one sparse problem per block, selecting exactly that block."""
+    npg = (p.context_lens.astype(np.int64) + p.page_size - 1) // p.page_size
+    stride = max(int(npg.max()), 1)
+    cuts = []
+    for r in range(p.num_seqs):
+        c = np.sort(rng.integers(0, npg[r] + 1, size=nparts - 1))
+        cuts.append(np.concatenate([[0], c, [npg[r]]]))
+    parts = []
+    for i in range(nparts):
+        sel = np.full((p.num_seqs, stride), -1, dtype=np.int32)
+        ns = np.zeros(p.num_seqs, dtype=np.int32)
+        for r in range(p.num_seqs):
+            pages = np.arange(cuts[r][i], cuts[r][i + 1], dtype=np.int32)
+            sel[r, :pages.size] = rng.permutation(pages)
+            ns[r] = pages.size
+        parts.append(_mutate(p, selected=sel, num_selected=ns))
+    return parts
+
+
+def pin_lse_merge_split_equals_whole(lib):
+    """Attention over a request's whole key set equals the log-sum-exp merge of the
+    attentions over disjoint parts of it (contiguous page blocks, some empty, with ragged
+    q_len, the causal cutoff, partial last pages and two KV heads), for the outputs and
+    the lse."""
+    p = _small(29, num_seqs=4, context_lens=[70, 33, 5, 100], q_lens=[3, 1, 2, 4],
+               num_kv_heads=2)
+    rng = np.random.default_rng(3)
+    for nparts in (2, 3, 5):
+        parts = _split_parts(p, nparts, rng)
+        outs, lses = zip(*[lib.decode(q) for q in parts])
+        mo, ml = lib.lse_merge(np.stack(outs), np.stack(lses))
+        wo, wl = lib.decode(p)
+        _close(mo, wo, 1e-12, f"merged output ({nparts} parts)")
+        _close(ml, wl, 1e-12, f"merged lse ({nparts} parts)")
+
+
+def pin_lse_merge_closed_forms(lib):
+    """One part is returned as it is; a part with lse -inf is ignored; two parts with equal
+    lse give the mean and lse + log 2, also at lse 1000 (the maximum is taken out before
+    exp); parts weighted e^1 : 1 give that mix; no finite part gives zeros and -inf."""
+    rng = np.random.default_rng(8)
+    o = rng.standard_normal((3, 2, 5, 8))
+    l = rng.standard_normal((3, 2, 5)) * 3
+    mo, ml = lib.lse_merge(o[:1], l[:1])
+    _close(mo, o[0], 0.0, "one part")
+    _close(ml, l[0], 0.0, "one part lse")
+    l2 = l.copy()
+    l2[1] = -np.inf
+    mo, ml = lib.lse_merge(o[:2], l2[:2])
+    _close(mo, o[0], 1e-15, "empty part ignored")
+    for base in (0.0, 1000.0):
+        le = np.full((2, 2, 5), base)
+        mo, ml = lib.lse_merge(o[:2], le)
+        _close(mo, (o[0] + o[1]) / 2, 1e-14, f"equal lse {base}")
+        _close(ml, le[0] + np.log(2.0), 1e-12, f"equal lse {base}: lse")
+    lw = np.stack([np.full((2, 5), 1.0), np.zeros((2, 5))])
+    mo, _ = lib.lse_merge(o[:2], lw)
+    e = np.e
+    _close(mo, (e * o[0] + o[1]) / (e + 1), 1e-14, "weights e : 1")
+    mo, ml = lib.lse_merge(o[:2], np.full((2, 2, 5), -np.inf))
+    assert np.all(mo == 0) and np.all(np.isneginf(ml)), "no finite part"
+
+
 # ---------------------------------------------------------- KV quantise-and-write (producer)
 
 def _finite_code_values():

@@ -54,6 +54,11 @@ MUTANTS = {
                           "const int64_t row = (page * num_kv_heads) * page_size + o;"),
     "quant_v_from_k": ("quantize_row(v_new + src,", "quantize_row(k_new + src,"),
     "quant_skips_counted": ("      ++bad;\n      continue;", "      continue;"),
+    "merge_exp_without_max": ("const double w = exp(l - M);", "const double w = exp(l);"),
+    "merge_lse_without_max": ("lse[v] = M + log(z);", "lse[v] = log(z);"),
+    "merge_unnormalised": ("for (int32_t d = 0; d < dim; ++d) o[d] /= z;", ""),
+    "merge_first_part_only": ("      if (l == -INFINITY) continue;\n      const double w",
+                              "      if (l == -INFINITY || i > 0) continue;\n      const double w"),
     "index_cutoff_off_by_one": ("int64_t lim = L - qlen + tok + 1;", "int64_t lim = L - qlen + tok;"),
     "index_natural_log": ("S[b] = m + log2(z);", "S[b] = m + log(z);"),
     "index_no_forced_page": ("if (nb > 0 && pb->topk > 0) sel[cnt++] = (int32_t)(nb - 1);", ""),
