@@ -1,12 +1,15 @@
 #!/usr/bin/env python
 """Benchmark of paged FP8-KV decode attention on GB300: one JSON line on rank 0.
 
-Metric: achieved HBM GB/s (algorithmic bytes / time; % of the measured peak) and query
-rows/s.  Default workload: dense decode at 8K -- batch 32, one KV head, 16 query heads
-per KV head, head_dim 128, pages of 128 tokens, every context 8192, q_len 1, per-token
-e4m3 K/V scales.  A step is one pa_decode call over the whole batch.  The timed region
-replays a CUDA graph of K back-to-back calls that cycle through several copies of the
-KV cache whose total exceeds 3x the L2, so that every call reads its KV from HBM.
+Metric: achieved HBM GB/s (algorithmic bytes / time; fraction of the measured peak) and
+query rows/s.  Headline workload: long-context decode at 128K -- batch 8, one KV head,
+16 query heads per KV head, head_dim 128, pages of 128 tokens, every context 131072,
+q_len 1, per-token e4m3 K/V scales.  A step is one pa_decode call over the whole batch.
+The timed region replays a CUDA graph of K back-to-back calls that cycle through several
+copies of the KV cache whose total exceeds 3x the L2, so that every call reads its KV
+from HBM.  The same run times the other decode workloads (dense 8K, 128K with a scalar
+scale, the BF16-KV control, ragged speculative decode, sparse selected pages and the
+per-token-as-decode prefill) and reports them under "workloads".
 
 --impl reference times the fp64 CPU oracle (the reference implementation of this
 build) on the host cores, on bounded samples of the same workload.
@@ -40,7 +43,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dense8k",
+    ap.add_argument("--workload", default="long128k",
                     choices=["dense8k", "bf16ctl", "long128k_scalar", "long128k", "ragged",
                              "sparse", "kv_write", "prefill", "indexer"])
     ap.add_argument("--partition", type=int, default=0, help="split-K partition tokens (0 = balanced)")
@@ -50,6 +53,10 @@ def parse():
                     help="FP8 plans with one query token: run the tcgen05 kernel (PA_PLAN_TCGEN05)")
     ap.add_argument("--profile", type=int, default=0,
                     help="only run --warmup + this many direct pa_decode calls (for ncu)")
+    ap.add_argument("--only", action="store_true",
+                    help="time the selected workload only (no 'workloads' key)")
+    ap.add_argument("--extra-steps", type=int, default=200,
+                    help="timed calls of each workload under 'workloads'")
     return ap.parse_args()
 
 
@@ -57,11 +64,7 @@ def parse():
 # from one ncu capture per workload, valid only for the kernel sources they were taken on
 # (sha256 over the code, comments stripped, of the C header and the decode kernels'
 # translation unit); any other code gives traffic null.
-MEASURED_TRAFFIC = {
-    "dense8k": {"bytes": 69465600 + 341248,
-                "csrc_sha256": "87d4317d84ae7d147e58b375373678d11489c1404418a80698ec2f2978247487",
-                "profile": "profiles/decode_kernel_dense8k_full.md"},
-}
+MEASURED_TRAFFIC = {}
 
 
 def _code_text(path):
@@ -90,11 +93,7 @@ def csrc_sha256():
 
 
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
-# Its DRAM writes at kernel end are below the bytes it writes: L2 still holds dirty lines
-# when the launch ends, and writes them back during the next one.
-MEASURED_TRAFFIC_KV_WRITE = {"bytes": 136342272 + 34774016,
-                             "src_sha256": "14ed1374fc2efcd4857c515ed043605f2b2a7e636b3e29abeaa2fb2fa2330c12",
-                             "profile": "profiles/kv_quantize_write_prefill8k_full.md"}
+MEASURED_TRAFFIC_KV_WRITE = {"bytes": None, "src_sha256": ""}
 
 
 def kv_write_sha256():
@@ -107,9 +106,9 @@ def kv_write_sha256():
     return h.hexdigest()
 
 
-def measured_traffic(workload):
+def measured_traffic(workload, sha=None):
     t = MEASURED_TRAFFIC.get(workload)
-    if not t or t["bytes"] is None or t["csrc_sha256"] != csrc_sha256():
+    if not t or t["bytes"] is None or t["csrc_sha256"] != (sha or csrc_sha256()):
         return None
     return t["bytes"]
 
@@ -237,6 +236,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def pre_queue(stream, cycles=2_000_000):
+    """A short device-side sleep (about a millisecond) ahead of the timed region's start
+    event, so that the host's launch of the CUDA graph after it is over before the device
+    reaches the event: the timed region holds device time only."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(cycles)
+
+
 def max_over_ranks(ms, world, dev):
     """The slowest rank's timed region (ms): every rank gets the maximum."""
     if world <= 1:
@@ -266,8 +274,8 @@ def time_oracle(p, target_s=10.0):
     """The oracle, as it stands, on all host cores: whole batches of p repeated until about
     target_s of wall time.  Returns (GB/s, rows/s, seconds, cores, passes)."""
     from oracle import oracle as O
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    cores = os.cpu_count() or 1
+    # the oracle threads over (request, KV head) pairs: no more threads than pairs do work
+    cores = max(1, min(os.cpu_count() or 1, p.num_seqs * p.num_kv_heads))
     passes = 0
     t0 = time.perf_counter()
     while True:
@@ -343,13 +351,13 @@ def bench_reference(args):
     if args.workload == "indexer":
         return bench_reference_indexer(args)
     p, desc = make_workload(args.workload)
-    cores = os.cpu_count() or 1
-    # Each step: `cores` requests of the workload, each truncated to n leading tokens, so
-    # that the whole --steps/--warmup run stays within about two minutes.
-    idx = list(range(min(cores, p.num_seqs)))
+    # Each step: up to one request per host core (the oracle threads over (request, KV
+    # head) pairs), each truncated to n leading tokens, so that the whole --steps/--warmup
+    # run stays within about two minutes.
+    idx = list(range(min(os.cpu_count() or 1, p.num_seqs)))
+    cores = max(1, len(idx) * p.num_kv_heads)
     from oracle import oracle as O
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_util import subset
+    from paged_fp8_kv_04_gb300.synth import subset
 
     def sample(n):
         q = subset(p, idx)
@@ -387,6 +395,123 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _decode_setup(name, dev, tcgen05=False, partition=0):
+    """Problem, plan and rotating KV copies of a decode workload on the device."""
+    import torch
+    from paged_fp8_kv_04_gb300 import device as dv
+    p, desc = make_workload(name)
+    d = dv.to_device(p, dev)
+    plan = dv.plan_for(p, device=dev, partition_tokens=partition, tcgen05=tcgen05)
+    total_bytes, kv_bytes = algorithmic_bytes(p)
+    # Rotating copies of the KV cache (and scales) so that no call finds its KV in L2.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool_bytes = sum(d[k].numel() * d[k].element_size() for k in
+                     ("k_cache", "v_cache", "k_scale", "v_scale") if d.get(k) is not None)
+    touched = max(kv_bytes, 1)
+    npools = max(3, int(math.ceil(3 * l2 / touched)) + 1)
+    npools = min(npools, max(3, int(40e9 // max(pool_bytes, 1))))
+    pools = [d] + [dict(d, **{k: d[k].clone() for k in ("k_cache", "v_cache", "k_scale", "v_scale")
+                              if d.get(k) is not None}) for _ in range(npools - 1)]
+    out = torch.empty(d["q"].shape, dtype=torch.bfloat16, device=dev)
+    keep = []
+    args_list = []
+    for pd in pools:
+        kw = dv.call_kwargs(p, pd)
+        args_list.append(plan.args(pd["q"], pd["k_cache"], pd["v_cache"], pd["block_table"],
+                                   pd["context_lens"], out=out, keep=keep, **kw))
+    # the copies were made on torch's stream; the decodes run on another one
+    torch.cuda.synchronize(dev)
+    # the pools stay referenced for as long as the argument blocks that point into them
+    return dict(p=p, desc=desc, d=d, plan=plan, total=total_bytes, kv=kv_bytes, npools=npools,
+                pool_bytes=pool_bytes, l2=l2, out=out, keep=keep, args_list=args_list,
+                pools=pools)
+
+
+def _graph_time(w, stream, dev, K, warmup, local, world=1):
+    """W direct calls, then a CUDA graph of back-to-back calls replayed until exactly K calls
+    ran inside the timed region (CUDA events on the launching stream, clocks sampled)."""
+    import torch
+    plan, args_list, npools = w["plan"], w["args_list"], w["npools"]
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            plan.decode_args(args_list[i % npools], stream=stream)
+    torch.cuda.synchronize(dev)
+    assert plan.device_status() == 0
+    chunk = max(c for c in range(1, min(K, 1000) + 1) if K % c == 0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            plan.decode_args(args_list[i % npools], stream=stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    pre_queue(stream)
+    with torch.cuda.stream(stream):  # CUDAGraph.replay launches on the current stream
+        e0.record(stream)
+        for _ in range(K // chunk):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    flags = plan.device_status()
+    del g
+    return ms, clk, flags
+
+
+def _prefill_roofline(p, us_per_call):
+    """The prefill rows share one sequence's pages, so the attended bytes come from L2
+    many times over: the bound is the contraction, 4 * D * g flops per attended token."""
+    flops = 4 * p.head_dim * p.group_size * p.num_kv_heads * int(p.context_lens.astype(np.int64).sum())
+    tf = flops / (us_per_call * 1e-6) / 1e12
+    tpeak = tensor_peak()
+    return {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
+            "frac": tf / tpeak, "traffic": None,
+            "peak_kind": "measured bf16_tflops (cuBLAS burst); f16 mma.sync runs below it"}
+
+
+def _extra_workloads(args, dev, stream, local, skip):
+    """Every other decode workload, timed the same way, for the 'workloads' key."""
+    import torch
+    peak, _ = peak_hbm()
+    sha = csrc_sha256()
+    res = {}
+    for name in ("dense8k", "long128k", "long128k_scalar", "bf16ctl", "ragged", "sparse", "prefill"):
+        if name == skip:
+            continue
+        w = _decode_setup(name, dev)
+        K = args.extra_steps
+        ms, clk, flags = _graph_time(w, stream, dev, K, args.warmup, local)
+        us = ms / K * 1e3
+        gbs = w["total"] / (us * 1e-6) / 1e9
+        info = w["plan"].info()
+        entry = {"workload": w["desc"], "us_per_call": us, "gbs": gbs, "frac": gbs / peak,
+                 "rows_per_s": w["p"].num_rows / (us * 1e-6), "steps": K,
+                 "algorithmic_bytes_per_call": int(w["total"]),
+                 "traffic": measured_traffic(name, sha), "grid_ctas": info["grid_ctas"],
+                 "stages": info["stages"], "clocks": clk, "device_flags": flags}
+        if name == "prefill":
+            entry["roofline"] = _prefill_roofline(w["p"], us)
+            entry["tokens_per_s"] = entry["rows_per_s"]
+        res[name] = entry
+        del w
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    return res
+
+
 def bench_ours(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -409,27 +534,10 @@ def bench_ours(args):
         return bench_kv_write(args, dev, rank, world, local)
     if args.workload == "indexer":
         return bench_indexer(args, dev, rank, world, local)
-    p, desc = make_workload(args.workload)
-    d = dv.to_device(p, dev)
-    plan = dv.plan_for(p, device=dev, partition_tokens=args.partition, tcgen05=args.tcgen05)
-    total_bytes, kv_bytes = algorithmic_bytes(p)
-
-    # Rotating copies of the KV cache (and scales) so that no call finds its KV in L2.
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool_bytes = sum(d[k].numel() * d[k].element_size() for k in
-                     ("k_cache", "v_cache", "k_scale", "v_scale") if d.get(k) is not None)
-    touched = max(kv_bytes, 1)
-    npools = max(3, int(math.ceil(3 * l2 / touched)) + 1)
-    npools = min(npools, max(3, int(40e9 // max(pool_bytes, 1))))
-    pools = [d] + [dict(d, **{k: d[k].clone() for k in ("k_cache", "v_cache", "k_scale", "v_scale")
-                              if d.get(k) is not None}) for _ in range(npools - 1)]
-    out = torch.empty(d["q"].shape, dtype=torch.bfloat16, device=dev)
-    keep = []
-    args_list = []
-    for pd in pools:
-        kw = dv.call_kwargs(p, pd)
-        args_list.append(plan.args(pd["q"], pd["k_cache"], pd["v_cache"], pd["block_table"],
-                                   pd["context_lens"], out=out, keep=keep, **kw))
+    w = _decode_setup(args.workload, dev, tcgen05=args.tcgen05, partition=args.partition)
+    p, desc, plan, d, out, keep = w["p"], w["desc"], w["plan"], w["d"], w["out"], w["keep"]
+    total_bytes, npools, args_list = w["total"], w["npools"], w["args_list"]
+    pool_bytes, l2 = w["pool_bytes"], w["l2"]
     stream = torch.cuda.Stream(device=dev)
 
     if args.profile:
@@ -441,48 +549,13 @@ def bench_ours(args):
                           "device_flags": plan.device_status()}), flush=True)
         return
 
-    # warm-up: W direct calls
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
-            plan.decode_args(args_list[i % npools], stream=stream)
-    torch.cuda.synchronize(dev)
-    assert plan.device_status() == 0
-
-    # one CUDA graph of `chunk` calls; the timed region replays it K / chunk times
     K = args.steps
-    chunk = max(c for c in range(1, min(K, 1000) + 1) if K % c == 0)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(chunk):
-            plan.decode_args(args_list[i % npools], stream=stream)
-    with torch.cuda.stream(stream):
-        g.replay()
-    torch.cuda.synchronize(dev)
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):  # CUDAGraph.replay launches on the current stream
-        e0.record(stream)
-        for _ in range(K // chunk):
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    ms = e0.elapsed_time(e1)
-    clk = clocks.stop()
-    flags = plan.device_status()
+    ms, clk, flags = _graph_time(w, stream, dev, K, args.warmup, local, world)
 
     # per-launch time of direct (non-graph) calls, for reference
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
-    nd = min(K, 2000)
+    nd = min(max(K, 20), 2000)
     with torch.cuda.stream(stream):
         e2.record(stream)
         for i in range(nd):
@@ -493,7 +566,6 @@ def bench_ours(args):
 
     t_max = max_over_ranks(ms, world, dev)
     value, rows_s = whole_job_rates(total_bytes, p.num_rows, K, world, t_max)
-    sec = t_max / 1e3
     us_per_call = ms / K * 1e3
 
     # end to end through the C ABI: pinned host inputs -> device, decode, output -> host
@@ -522,6 +594,14 @@ def bench_ours(args):
         e2e = {"value": world * total_bytes / dt / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": dt * 1e3}
+        del host, dbuf, hout
+
+    info = plan.info()
+    extra = None
+    if not args.only and args.partition == 0 and not args.tcgen05:
+        del w, d, out, keep, args_list, plan
+        torch.cuda.empty_cache()
+        extra = _extra_workloads(args, dev, stream, local, args.workload)
 
     if rank != 0:
         return
@@ -533,7 +613,6 @@ def bench_ours(args):
         cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"the full batch ({p.num_rows} rows) {passes} times, {dt:.1f} s wall",
                "rows_per_s": rps}
-    info = plan.info()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t_max / K, "higher_is_better": True,
@@ -541,7 +620,7 @@ def bench_ours(args):
         if p.kv_dtype == "fp8" else "bf16 mma, f32 accumulate", "data": "synthetic",
         "config": {"workload": desc, "l2": f"{npools} rotating KV copies ({npools * pool_bytes / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB)",
                    "timed": "CUDA graph replay of back-to-back pa_decode calls",
-                   "kernel": "tcgen05" if args.tcgen05 and plan.info()["kernel"] == 1 else "mma.sync",
+                   "kernel": "tcgen05" if info["kernel"] == 1 else "mma.sync",
                    "grid_ctas": info["grid_ctas"], "stages": info["stages"],
                    "partition_tokens": args.partition},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -555,16 +634,11 @@ def bench_ours(args):
         "device_flags": flags,
     }
     if args.workload == "prefill":
-        # The rows share one sequence's pages, so the attended bytes come from L2 many
-        # times over: the bound is the contraction, 4 * D * g flops per attended token.
-        flops = 4 * p.head_dim * p.group_size * p.num_kv_heads * int(p.context_lens.astype(np.int64).sum())
-        tf = flops / (us_per_call * 1e-6) / 1e12
-        tpeak = tensor_peak()
-        line["roofline"] = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
-                            "frac": tf / tpeak, "traffic": None,
-                            "peak_kind": "measured bf16_tflops (cuBLAS burst); f16 mma.sync runs below it"}
+        line["roofline"] = _prefill_roofline(p, us_per_call)
         line["attended_bytes_per_s_note"] = "value counts attended KV bytes, most served from L2"
         line["tokens_per_s"] = rows_s
+    if extra is not None:
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
 
 
@@ -623,6 +697,7 @@ def bench_indexer(args, dev, rank, world, local):
     time.sleep(0.3)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    pre_queue(stream)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(K // chunk):
@@ -717,6 +792,7 @@ def bench_kv_write(args, dev, rank, world, local):
     time.sleep(0.3)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    pre_queue(stream)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(K // chunk):
@@ -782,7 +858,8 @@ def bench_kv_write(args, dev, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": (MEASURED_TRAFFIC_KV_WRITE["bytes"]
-                                 if MEASURED_TRAFFIC_KV_WRITE["src_sha256"] == kv_write_sha256()
+                                 if MEASURED_TRAFFIC_KV_WRITE["bytes"] is not None and
+                                 MEASURED_TRAFFIC_KV_WRITE["src_sha256"] == kv_write_sha256()
                                  else None),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": K, "clocks": clk,

@@ -5,7 +5,8 @@
  * with a log-sum-exp merge, and a sparse selected-page variant; with the two steps next
  * to it: the per-token FP8 quantise-and-write that fills the cache
  * (pa_kv_quantize_write) and the indexer's page scores and top-k that choose the sparse
- * variant's pages (pa_index_topk).  sm_103a (GB300).
+ * variant's pages (pa_index_topk); and the log-sum-exp merge that combines the parts of a
+ * context split across GPUs (pa_lse_merge).  sm_103a (GB300).
  *
  * Sources of the operation (the pages are pull-request threads):
  *  - ROCm/ATOM PR 2614, "Change": dense max-q-len-1 per-token FP8 decode and sparse
@@ -317,6 +318,40 @@ typedef struct pa_index_args {
  * PA_ERR_UNSUPPORTED for head_dim, page_size or max_q_len * index_heads outside the
  * limits above, PA_ERR_CUDA when a launch fails. */
 pa_status_t pa_index_topk(const pa_index_args_t *args, void *stream);
+
+/* ---- the merge of a context split across GPUs ---- */
+
+/* Arguments of pa_lse_merge.  All pointers are device pointers. */
+typedef struct pa_lse_merge_args {
+  const float *part_out;   /* fp32 [num_parts, num_rows, num_heads, head_dim]: each part's normalised
+                              attention output (pa_decode with PA_OUT_F32), 16-B aligned */
+  const float *part_lse;   /* fp32 [num_parts, num_rows, num_heads]: each part's natural-log LSE
+                              (pa_decode's lse; -inf where the part attended no position) */
+  void *out;               /* [num_rows, num_heads, head_dim], bf16 or fp32 per out_dtype, 16-B aligned */
+  float *lse;              /* fp32 [num_rows, num_heads] merged LSE, or NULL */
+  int32_t num_parts;       /* 1 .. 64 */
+  int32_t num_rows;        /* >= 0; 0 enqueues nothing */
+  int32_t num_heads;       /* >= 1 */
+  int32_t head_dim;        /* 128 */
+  int32_t out_dtype;       /* PA_OUT_BF16 (round to nearest even) or PA_OUT_F32 */
+  int32_t reserved;        /* 0 */
+} pa_lse_merge_args_t;
+
+/* Merges attention partials computed over disjoint parts of each request's positions: the
+ * combine step of a long context split across GPUs (each GPU decodes its own pages with
+ * pa_decode, PA_OUT_F32 and an lse; the parts are gathered, then merged here).  It is the
+ * merge of the split-K partition triple -- maximum logit, exponential sum and partial
+ * output per partition, ROCm/ATOM PR 2710, "Smaller" -- with each part's (max, sum) carried
+ * as its lse; MiniMax-M3 is served across four GPUs (ROCm/ATOM PR 2614, "Validation").
+ * For every (row, head) v, over the parts i with lse_i > -inf:
+ *   M = max_i lse_i, w_i = exp(lse_i - M),
+ *   out[v] = sum_i w_i part_out_i[v] / sum_i w_i,   lse[v] = M + log sum_i w_i;
+ * no such part gives out = 0 and lse = -inf (an empty part's output is never read).
+ * One kernel launch on `stream`; no host synchronisation, no allocation.
+ * PA_ERR_INVALID_ARG for a missing pointer or a bad size, PA_ERR_ALIGN for a misaligned
+ * pointer, PA_ERR_UNSUPPORTED for head_dim other than 128 or more than 64 parts,
+ * PA_ERR_CUDA when the launch fails. */
+pa_status_t pa_lse_merge(const pa_lse_merge_args_t *args, void *stream);
 
 /* ---- test hooks: exact integer / byte outputs of the row map and the page gather ---- */
 

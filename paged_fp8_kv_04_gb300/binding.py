@@ -91,6 +91,14 @@ class IndexArgs(ctypes.Structure):
                 ("block_table_stride", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
                 ("sm_scale", ctypes.c_float), ("reserved", ctypes.c_int32)]
 
+class LseMergeArgs(ctypes.Structure):
+    _fields_ = [("part_out", ctypes.c_void_p), ("part_lse", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("num_parts", ctypes.c_int32), ("num_rows", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _lib = None
 P = ctypes.c_void_p
 
@@ -142,6 +150,8 @@ def lib(path: Optional[str] = None):
     L.pa_kv_quantize_write.restype = ctypes.c_int
     L.pa_index_topk.argtypes = [ctypes.POINTER(IndexArgs), P]
     L.pa_index_topk.restype = ctypes.c_int
+    L.pa_lse_merge.argtypes = [ctypes.POINTER(LseMergeArgs), P]
+    L.pa_lse_merge.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L
@@ -376,3 +386,27 @@ def index_topk(args: IndexArgs, device=None, stream=None) -> None:
     st = lib().pa_index_topk(ctypes.byref(args), ctypes.c_void_p(s.cuda_stream))
     if st != 0:
         raise PaError(st, "pa_index_topk")
+
+
+def lse_merge_args(part_out, part_lse, out, lse=None) -> LseMergeArgs:
+    """pa_lse_merge_args_t over torch tensors: part_out fp32 [parts, rows, heads, D],
+    part_lse fp32 [parts, rows, heads], out bf16 or fp32 [rows, heads, D], lse fp32
+    [rows, heads] or None."""
+    import torch
+    a = LseMergeArgs()
+    a.part_out, a.part_lse, a.out, a.lse = _ptr(part_out), _ptr(part_lse), _ptr(out), _ptr(lse)
+    a.num_parts, a.num_rows, a.num_heads, a.head_dim = (int(x) for x in part_out.shape)
+    a.out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    a.reserved = 0
+    return a
+
+
+def lse_merge(part_out, part_lse, out, lse=None, stream=None, args: Optional[LseMergeArgs] = None):
+    """Enqueues pa_lse_merge on `stream` (default: torch's current stream); returns out."""
+    import torch
+    a = args if args is not None else lse_merge_args(part_out, part_lse, out, lse)
+    s = stream if stream is not None else torch.cuda.current_stream(out.device)
+    st = lib().pa_lse_merge(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
+    if st != 0:
+        raise PaError(st, "pa_lse_merge")
+    return out

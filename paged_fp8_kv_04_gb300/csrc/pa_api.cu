@@ -22,13 +22,15 @@ namespace {
 constexpr int kMaxBatch = 4096;
 constexpr int kMaxSmemDefault = 232448;  // 227 KB opt-in per CTA on sm_100-class parts
 constexpr double kLog2e = 1.4426950408889634;
+constexpr int kSmallXSlots = 2;  // exchange slots of plans with at most two query tokens
 
 struct Geometry {
   int num_sms = 0, grid = 0, nstage = 0, ppt = 0, ps_shift = 0, mmax = 0;
   int maxch = 0, part_tiles = 0, max_tiles = 0, stage_bytes = 0, qslot_bytes = 0;
   int off_q = 0, off_merge = 0, off_tstart = 0, off_meta = 0, off_bar = 0, off_misc = 0;
+  int xslots = 4;
   int64_t slots = 0;
-  size_t smem = 0, ws = 0, off_status = 0, off_counters = 0, off_ml = 0, off_o = 0;
+  size_t smem = 0, ws = 0, off_status = 0, off_counters = 0, off_flags = 0, off_ml = 0, off_o = 0;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -90,6 +92,8 @@ pa_status_t device_sms(int *sms, int *smem_optin) {
   return PA_OK;
 }
 
+bool use_umma(const pa_plan_desc_t &d);
+
 pa_status_t geometry(const pa_plan_desc_t *d, Geometry *g) {
   pa_status_t st = validate(d);
   if (st != PA_OK) return st;
@@ -121,12 +125,17 @@ pa_status_t geometry(const pa_plan_desc_t *d, Geometry *g) {
   g->stage_bytes = d->kv_dtype == PA_KV_FP8_E4M3 ? (2 * pa::kTile * pa::kD + 1024)
                                                  : (4 * pa::kTile * pa::kD);
   g->qslot_bytes = d->q_len * pa::kQRowBytes;
+  // the exchange buffer (mid-stream ends; the CTA's last merge runs in stage memory): 4
+  // slots, or 2 for plans of at most two query tokens on the mma.sync kernel (a round moves
+  // whole slices, q_len m-tiles each), which leaves room for one more stage
+  g->xslots = (d->q_len <= 2 && !use_umma(*d)) ? kSmallXSlots : 4;
+  const size_t merge_bytes = (size_t)g->xslots * (8192 + 512);
   for (int ns = 6; ns >= 2; --ns) {
     size_t off = (size_t)ns * g->stage_bytes;
     const size_t off_q = off;
     off += 2 * (size_t)g->qslot_bytes;
     const size_t off_merge = off;
-    off += pa::kMergeBytes;
+    off += merge_bytes;
     const size_t off_tstart = off;
     off += round_up((size_t)(2 * d->max_batch + 4) * 4, 16);  // tstart, then the CTA prefix
     const size_t off_meta = off;
@@ -154,6 +163,8 @@ pa_status_t geometry(const pa_plan_desc_t *d, Geometry *g) {
   g->off_status = off;
   off += 256;
   g->off_counters = off;
+  off = round_up(off + (size_t)d->max_batch * d->num_kv_heads * 4, 256);
+  g->off_flags = off;
   off = round_up(off + (size_t)d->max_batch * d->num_kv_heads * 4, 256);
   g->off_ml = off;
   off = round_up(off + (size_t)g->slots * 2 * g->mmax * 4, 256);
@@ -275,6 +286,7 @@ void fill_params(const pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k)
   k->lse = a->lse;
   k->status = reinterpret_cast<uint32_t *>(ws + g.off_status);
   k->counters = reinterpret_cast<int32_t *>(ws + g.off_counters);
+  k->flags = reinterpret_cast<int32_t *>(ws + g.off_flags);
   k->part_ml = reinterpret_cast<float *>(ws + g.off_ml);
   k->part_o = reinterpret_cast<float *>(ws + g.off_o);
   k->dump = nullptr;
@@ -290,14 +302,14 @@ void fill_params(const pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k)
     // output once (vLLM PR 52060, "Suggested Fix").
     k->kfold = (float)((double)a->k_scale_scalar * sl2);
     k->pfold = 1.f;
-    k->vpost = a->v_scale_scalar;
+    k->vpost = a->v_scale_scalar * (1.f / 256.f);  // P' of the mma.sync kernel carries 2^8
   } else {
     // Per-token scales: k_scale[token] multiplies the score column, v_scale[token] the
-    // P column.  P' = p * v_scale * 256 keeps the f16 P operand in its normal range
-    // (v_scale ~ amax / 448); the exact power of two is undone on the output.
+    // P column, relative to a power of two that the kernel keeps per warp and undoes
+    // before the output.
     k->kfold = (float)sl2;
-    k->pfold = 256.f;
-    k->vpost = 1.f / 256.f;
+    k->pfold = 1.f;
+    k->vpost = 1.f;
   }
   k->num_seqs = a->num_seqs;
   k->Hkv = d.num_kv_heads;
@@ -315,6 +327,9 @@ void fill_params(const pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k)
   k->part_tiles = g.part_tiles;
   k->maxch = g.maxch;
   k->grid = d.partition_tokens > 0 ? a->num_seqs * d.num_kv_heads * g.maxch : g.grid;
+  // one CTA per SM (the launch bound and the shared-memory carve allow no more), so a grid
+  // no larger than the SM count is resident at once
+  k->coresident = k->grid <= g.num_sms ? 1 : 0;
   k->nstage = g.nstage;
   k->mmax = g.mmax;
   k->sparse = a->selected_pages != nullptr;
@@ -326,6 +341,7 @@ void fill_params(const pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k)
   k->off_bar = g.off_bar;
   k->off_misc = g.off_misc;
   k->stage_bytes = g.stage_bytes;
+  k->xslots = g.xslots;
 }
 
 pa_status_t tensor_maps(pa_plan *plan, const pa_decode_args_t *a, pa::KParams *k) {
@@ -376,8 +392,10 @@ cudaError_t launch_umma(const pa::KParams &k, size_t smem, cudaStream_t s, bool 
   cfg.numAttrs = pdl ? 1 : 0;
   pa::KParams ku = k;
   // The tcgen05 kernel folds the per-token V scale into P relative to its maximum and
-  // undoes the 256 of P's range itself: only the scalar V scale is left for the end.
+  // undoes the 256 of P's range itself: only the scalar V scale is left for the end
+  // (without the mma.sync kernel's 2^-8).
   if (SM == PA_SCALE_PER_TOKEN) ku.vpost = 1.f;
+  if (SM == PA_SCALE_SCALAR) ku.vpost = k.vpost * 256.f;
   return cudaLaunchKernelEx(&cfg, pa::decode_umma_kernel<SM>, ku);
 }
 
@@ -575,6 +593,7 @@ pa_status_t pa_debug_row_map(pa_plan_t *plan, const pa_decode_args_t *args, int3
   if (plan->ws == nullptr) return PA_ERR_WORKSPACE;
   fill_params(plan, args, &k);
   const int blocks = (args->num_seqs + 127) / 128;
+  (void)cudaGetLastError();  // drop an earlier, unrelated launch error
   pa::row_map_kernel<<<blocks, 128, 0, static_cast<cudaStream_t>(stream)>>>(k, row_map);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -638,6 +657,9 @@ void noalloc_setup(NoAllocDevice &nd) {
   for (int m = 0; m < 3 && e == cudaSuccess; ++m) {
     d.kv_dtype = modes[m][0];
     d.scale_mode = modes[m][1];
+    // q_len 1 with the tcgen05 flag raises the tcgen05 kernels' limit too (for FP8 modes)
+    d.q_len = 1;
+    d.flags = PA_PLAN_TCGEN05;
     e = prepare_kernels(d, (size_t)smem_optin);
   }
   nd.ptr = ptr;

@@ -28,6 +28,8 @@ struct Frag {
   uint32_t qf[8][4];
   float o[16][4];
   float m[2], l[2];
+  int pe[2];  // per-token V scales: row g's (pe[0]) and row g + 8's (pe[1]) o and P' are in
+              // units of 2^pe (online_row_pe)
 };
 
 __device__ __forceinline__ float quad_sum(float v) {
@@ -98,17 +100,140 @@ __device__ __forceinline__ void reset_state(Frag &f) {
     for (int e = 0; e < 4; ++e) f.o[i][e] = 0.f;
   f.m[0] = f.m[1] = -INFINITY;
   f.l[0] = f.l[1] = 0.f;
+  f.pe[0] = f.pe[1] = 0;
+}
+
+// Per-token V scales fold into P per row: P'[j] = p[j] * v_scale[j] * 2^pe, with one power
+// of two per row (and lane quad).  When it is set, the chunk's largest p * v_scale * 2^pe
+// lands in [2^6, 2^7); it is kept while that stays within [2^-6, 2^12).  So P' never
+// overflows the f16 operand, and the largest terms of every chunk keep f16's 11 bits,
+// however far apart the tokens' magnitudes (per-token scales of 2^-20 .. 2^20 in one
+// sequence included): the reference is the largest product, not the largest scale, so a
+// token with p = 1 and a small scale is not flushed by a neighbour with a large scale and
+// p ~ 0.  The row's o is accumulated in the same units.  The power of two rides in the
+// exponent of p (online_row_pe), so the common case costs one multiply per term, as a
+// fixed fold would; pe stays within [-60, 60], which covers V scales of 2^-60 .. 2^64.
+constexpr int kPeMin = -60, kPeMax = 60;
+constexpr int kScalarPe = 8;  // the fixed power of two of P in scalar-scale mode
+
+// online_row with p' = 2^(s - m + pe) = p * 2^pe in s on return; l still sums p.
+template <int N>
+__device__ __forceinline__ float online_row_pe(float (&s)[N], float &m, float &l, int pe) {
+  float mx = s[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) mx = fmaxf(mx, s[k]);
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
+  float alpha = 1.f;
+  if (mx > m) {
+    alpha = fast_exp2(m - mx);
+    m = mx;
+    l *= alpha;
+  }
+  const float ref = ((m == -INFINITY) ? 0.f : m) - (float)pe;
+#pragma unroll
+  for (int k = 0; k < N; ++k) s[k] = fast_exp2(s[k] - ref);
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; k += 4) sum += (s[k] + s[k + 1]) + (s[k + 2] + s[k + 3]);
+  l += sum * __uint_as_float((uint32_t)(127 - pe) << 23);
+  return alpha;
+}
+
+// The largest of this lane's P' of row g (half 0) and row g + 8 (half 1) in the packed f16
+// fragments, as an f16x2 word, reduced over the lane quad (which holds the rows' columns).
+template <int NKS>
+__device__ __forceinline__ uint32_t packed_row_max(const uint32_t (&pa)[NKS][4]) {
+  uint32_t r0 = hmax2(pa[0][0], pa[0][2]), r1 = hmax2(pa[0][1], pa[0][3]);
+#pragma unroll
+  for (int ks = 1; ks < NKS; ++ks) {
+    r0 = hmax2(r0, hmax2(pa[ks][0], pa[ks][2]));
+    r1 = hmax2(r1, hmax2(pa[ks][1], pa[ks][3]));
+  }
+  // (lo, hi) of each row -> one word: row g's maximum in the low half, row g + 8's in the high
+  uint32_t w = hmax2(prmt(r0, r1, 0x5410), prmt(r0, r1, 0x7632));
+  w = hmax2(w, __shfl_xor_sync(~0u, w, 1));
+  w = hmax2(w, __shfl_xor_sync(~0u, w, 2));
+  return w;
+}
+
+// An f16 row maximum inside [2^-6, 2^12): 0x2400 <= bits < 0x6C00 (sign clear; f16's
+// exponent field holds e + 15).
+__device__ __forceinline__ bool in_window(uint32_t h) { return h >= 0x2400u && h < 0x6C00u; }
+
+// The row's P' (in s, fp32) left its window: a new pe from the fp32 maximum (0 keeps it).
+// Returns the factor P' and the row's o are rescaled by.
+template <int N>
+__device__ __forceinline__ float refold_row(float (&s)[N], int &pe) {
+  float wmax = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; ++k) wmax = fmaxf(wmax, s[k]);
+  wmax = fmaxf(wmax, __shfl_xor_sync(~0u, wmax, 1));
+  wmax = fmaxf(wmax, __shfl_xor_sync(~0u, wmax, 2));
+  float rs = 1.f;
+  if (wmax > 0.f) {
+    const int ev = (int)((__float_as_uint(wmax) >> 23) & 0xFFu) - 127;  // floor(log2 wmax)
+    if (ev < -6 || ev > 11) {
+      const int ne = min(min(max(pe + 6 - ev, kPeMin), kPeMax), pe + 64);
+      const int d = ne - pe;
+      rs = d < -126 ? 0.f : __uint_as_float((uint32_t)(d + 127) << 23);
+      pe = ne;
+#pragma unroll
+      for (int k = 0; k < N; ++k) s[k] *= rs;
+    }
+  }
+  return rs;
+}
+
+// o back to plain units (2^-pe per row, exact) before it leaves the warp.
+__device__ __forceinline__ void unfold_rows(Frag &f) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    if (f.pe[hf] == 0) continue;
+    const float u = __uint_as_float((uint32_t)(127 - f.pe[hf]) << 23);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      f.o[i][2 * hf] *= u;
+      f.o[i][2 * hf + 1] *= u;
+    }
+    f.pe[hf] = 0;
+  }
 }
 
 // ------------------------------------------------------------------------ online softmax
 
-// s holds the log2-domain scores of this lane's 8 columns of one row (tokens
-// 8j + 2t + e of the chunk's n-tiles j = 0..3, column 2j + e); on return it holds
-// p = 2^(s - m) with m the row's running maximum.  Rescales l and the row's
-// accumulators (o[.][half], o[.][half + 1]) when the maximum grows.
+// s holds the log2-domain scores of this lane's columns of one row (tokens 8j + 2t + e
+// of the chunk's n-tiles j, column 2j + e); on return it holds p = 2^(s - m) with m the
+// row's running maximum, and l is updated.  Returns the factor by which the row's
+// accumulators must be rescaled (1 when the maximum did not grow).
 template <int N>
-__device__ __forceinline__ void online_row(float (&s)[N], float &m, float &l, float (&o)[16][4],
-                                           int half) {
+__device__ __forceinline__ float online_row(float (&s)[N], float &m, float &l) {
+  float mx = s[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) mx = fmaxf(mx, s[k]);
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
+  float alpha = 1.f;
+  if (mx > m) {
+    alpha = fast_exp2(m - mx);
+    m = mx;
+    l *= alpha;
+  }
+  const float ref = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+  for (int k = 0; k < N; ++k) s[k] = fast_exp2(s[k] - ref);
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; k += 4) sum += (s[k] + s[k + 1]) + (s[k + 2] + s[k + 3]);
+  l += sum;
+  return alpha;
+}
+
+// online_row, then the rescale of the row's accumulators (o[.][half], o[.][half + 1]) in
+// the same branch, for paths whose P needs no further fold.
+template <int N>
+__device__ __forceinline__ void online_row_rescale(float (&s)[N], float &m, float &l,
+                                                   float (&o)[16][4], int half) {
   float mx = s[0];
 #pragma unroll
   for (int k = 1; k < N; ++k) mx = fmaxf(mx, s[k]);
@@ -131,6 +256,24 @@ __device__ __forceinline__ void online_row(float (&s)[N], float &m, float &l, fl
 #pragma unroll
   for (int k = 0; k < N; k += 4) sum += (s[k] + s[k + 1]) + (s[k + 2] + s[k + 3]);
   l += sum;
+}
+
+// Rescales the accumulators of row g by a0 and of row g + 8 by a1.
+__device__ __forceinline__ void rescale_rows(float (&o)[16][4], float a0, float a1) {
+  if (a0 != 1.f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][0] *= a0;
+      o[i][1] *= a0;
+    }
+  }
+  if (a1 != 1.f) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][2] *= a1;
+      o[i][3] *= a1;
+    }
+  }
 }
 
 // Masks the columns whose position is not below the row's cutoff.  pos0[h] is the
@@ -162,23 +305,23 @@ __device__ __forceinline__ void mask_weights(float (&w)[N], const int (&pos0)[N 
   }
 }
 
-// P fragments of the chunk's two PV k-steps from the probabilities (per-column scale w).
+// P fragments of the chunk's PV k-steps from P' of rows g (s0) and g + 8 (s1).
 template <int N>
-__device__ __forceinline__ void pack_p(const float (&s0)[N], const float (&s1)[N],
-                                       const float (&w)[N], bool bf16, uint32_t (&pa)[N / 4][4]) {
+__device__ __forceinline__ void pack_p(const float (&s0)[N], const float (&s1)[N], bool bf16,
+                                       uint32_t (&pa)[N / 4][4]) {
 #pragma unroll
   for (int ks = 0; ks < N / 4; ++ks) {
     const int c = 4 * ks;
     if (bf16) {
-      pa[ks][0] = pack_bf16x2(s0[c] * w[c], s0[c + 1] * w[c + 1]);
-      pa[ks][1] = pack_bf16x2(s1[c] * w[c], s1[c + 1] * w[c + 1]);
-      pa[ks][2] = pack_bf16x2(s0[c + 2] * w[c + 2], s0[c + 3] * w[c + 3]);
-      pa[ks][3] = pack_bf16x2(s1[c + 2] * w[c + 2], s1[c + 3] * w[c + 3]);
+      pa[ks][0] = pack_bf16x2(s0[c], s0[c + 1]);
+      pa[ks][1] = pack_bf16x2(s1[c], s1[c + 1]);
+      pa[ks][2] = pack_bf16x2(s0[c + 2], s0[c + 3]);
+      pa[ks][3] = pack_bf16x2(s1[c + 2], s1[c + 3]);
     } else {
-      pa[ks][0] = pack_f16x2(s0[c] * w[c], s0[c + 1] * w[c + 1]);
-      pa[ks][1] = pack_f16x2(s1[c] * w[c], s1[c + 1] * w[c + 1]);
-      pa[ks][2] = pack_f16x2(s0[c + 2] * w[c + 2], s0[c + 3] * w[c + 3]);
-      pa[ks][3] = pack_f16x2(s1[c + 2] * w[c + 2], s1[c + 3] * w[c + 3]);
+      pa[ks][0] = pack_f16x2(s0[c], s0[c + 1]);
+      pa[ks][1] = pack_f16x2(s1[c], s1[c + 1]);
+      pa[ks][2] = pack_f16x2(s0[c + 2], s0[c + 3]);
+      pa[ks][3] = pack_f16x2(s1[c + 2], s1[c + 3]);
     }
   }
 }
@@ -187,13 +330,13 @@ __device__ __forceinline__ void pack_p(const float (&s0)[N], const float (&s1)[N
 
 // FP8 tile: K at st, V at st + 16384 (each [128 tokens][128 B], 128-byte swizzle),
 // K scales at st + 32768, V scales at st + 33280 (fp32 per token).  Tokens tb ..
-// tb + 32 NCH - 1.  With NCH = 2 the warp holds two independent chains per step (8 QK
-// n-tiles, 4 PV k-steps), which keeps the tensor and conversion pipes busier per warp.
-template <int SM, int NCH>
+// tb + 8 NJ - 1: NJ QK n-tiles of 8 tokens (NJ independent accumulator chains) and NJ / 2
+// PV k-steps of 16 tokens.
+template <int SM, int NJ>
 __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb, bool masked,
-                                          const int (&pos0)[2 * NCH], int cut, int Lctx, int g,
+                                          const int (&pos0)[NJ / 2], int cut, int Lctx, int g,
                                           int t, Frag &f) {
-  constexpr int NJ = 4 * NCH, NC = 2 * NJ, NKS = 2 * NCH;
+  constexpr int NC = 2 * NJ, NKS = NJ / 2;
   const uint32_t Kb = st, Vb = st + 16384;
   const uint32_t sw0 = ((2 * t) ^ g) << 4, sw1 = ((2 * t + 1) ^ g) << 4;
   uint32_t w[NJ][8];
@@ -224,8 +367,8 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
       const float2 y = lds64f(st + 33280 + (tb + 8 * j + 2 * t) * 4);
       c[2 * j] = x.x * p.kfold;
       c[2 * j + 1] = x.y * p.kfold;
-      vw[2 * j] = y.x * p.pfold;
-      vw[2 * j + 1] = y.y * p.pfold;
+      vw[2 * j] = y.x;
+      vw[2 * j + 1] = y.y;
     }
   } else {
 #pragma unroll
@@ -246,10 +389,31 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
     mask_scores<NC>(s0, s1, pos0, cut);
     if (SM == PA_SCALE_PER_TOKEN) mask_weights<NC>(vw, pos0, cut);
   }
-  online_row<NC>(s0, f.m[0], f.l[0], f.o, 0);
-  online_row<NC>(s1, f.m[1], f.l[1], f.o, 2);
   uint32_t pa[NKS][4];
-  pack_p<NC>(s0, s1, vw, false, pa);
+  if (SM == PA_SCALE_PER_TOKEN) {
+    float a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], f.pe[0]);
+    float a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], f.pe[1]);
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      s0[k] *= vw[k];
+      s1[k] *= vw[k];
+    }
+    pack_p<NC>(s0, s1, false, pa);
+    const uint32_t wm = packed_row_max<NKS>(pa);
+    if (__any_sync(~0u, !(in_window(wm & 0xFFFFu) && in_window(wm >> 16)))) {  // rare
+      a0 *= refold_row<NC>(s0, f.pe[0]);
+      a1 *= refold_row<NC>(s1, f.pe[1]);
+      pack_p<NC>(s0, s1, false, pa);
+    }
+    rescale_rows(f.o, a0, a1);
+  } else {
+    // one scale for the whole cache: P' = p * 2^8 (p <= 1) keeps p down to 2^-22 out of
+    // f16's subnormals; the host folds 2^-8 into the V scale applied at the end
+    const float a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], kScalarPe);
+    const float a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], kScalarPe);
+    rescale_rows(f.o, a0, a1);
+    pack_p<NC>(s0, s1, false, pa);
+  }
 #pragma unroll
   for (int ks = 0; ks < NKS; ++ks) {
     const int rv = tb + 16 * ks + 2 * t;
@@ -307,20 +471,19 @@ __device__ __forceinline__ void chunk_bf16(const KParams &p, uint32_t st, int tb
     }
   }
   const float k = p.kfold;
-  float s0[8], s1[8], vw[8];
+  float s0[8], s1[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     s0[2 * j] = acc[j][0] * k;
     s0[2 * j + 1] = acc[j][1] * k;
     s1[2 * j] = acc[j][2] * k;
     s1[2 * j + 1] = acc[j][3] * k;
-    vw[2 * j] = vw[2 * j + 1] = 1.f;
   }
   if (masked) mask_scores<8>(s0, s1, pos0, cut);
-  online_row<8>(s0, f.m[0], f.l[0], f.o, 0);
-  online_row<8>(s1, f.m[1], f.l[1], f.o, 2);
+  online_row_rescale<8>(s0, f.m[0], f.l[0], f.o, 0);
+  online_row_rescale<8>(s1, f.m[1], f.l[1], f.o, 2);
   uint32_t pa[2][4];
-  pack_p<8>(s0, s1, vw, true, pa);
+  pack_p<8>(s0, s1, true, pa);
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
     const int tok = tb + 16 * ks + 8 * (mat & 1) + rr;
@@ -344,9 +507,10 @@ __device__ __forceinline__ void chunk_bf16(const KParams &p, uint32_t st, int tb
 
 // ------------------------------------------------------------------------ state exchange
 
-// Merge-buffer slot k: accumulators as [16][32 lanes][4] floats, then m0, m1, l0, l1.
+// Exchange-buffer slot k: accumulators as [16][32 lanes][4] floats at k * 8 KB; the lanes'
+// (m0, m1, l0, l1) in a 512-byte block per slot after all slots' accumulators.
 __device__ __forceinline__ void put_state(const Smem &sm, int k, const Frag &f, int lane) {
-  const uint32_t ob = sm.merge() + k * 8192, mb = sm.merge() + 32768 + k * 512;
+  const uint32_t ob = sm.merge() + k * 8192, mb = sm.merge_ml_at(k);
 #pragma unroll
   for (int i = 0; i < 16; ++i)
     sts128(ob + (i * 32 + lane) * 16,
@@ -359,7 +523,7 @@ __device__ __forceinline__ void put_state(const Smem &sm, int k, const Frag &f, 
 }
 
 __device__ __forceinline__ void merge_state(const Smem &sm, int k, Frag &f, int lane) {
-  const uint32_t ob = sm.merge() + k * 8192, mb = sm.merge() + 32768 + k * 512;
+  const uint32_t ob = sm.merge() + k * 8192, mb = sm.merge_ml_at(k);
   float v[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
@@ -550,10 +714,145 @@ __device__ void merge_partials(const KParams &p, int h, int row0, int qlen, int 
   }
 }
 
-// Merges several exchange slots (k0 .. k0 + cnt - 1) into this warp's state.
-__device__ __forceinline__ void merge_states(const Smem &sm, int k0, int cnt, int stride, Frag &f,
-                                             int lane) {
-  for (int j = 0; j < cnt; ++j) merge_state(sm, k0 + j * stride, f, lane);
+// ------------------------------------------------------- merges at the end of a sequence
+
+// An exchange slot in stage memory (at the CTA's last sequence end, when no tile is in
+// flight): the warp's accumulators as [16][32 lanes][4] floats (fragment order), then per
+// lane (m_g, m_g+8, L_g, L_g+8) with L the row's sum over the lane quad.
+constexpr int kSlotBytes = 8192 + 512;
+constexpr int kMaxSlots = 8;
+
+__device__ __forceinline__ void put_slot(uint32_t base, const Frag &f, int lane) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    sts128(base + (i * 32 + lane) * 16,
+           make_uint4(__float_as_uint(f.o[i][0]), __float_as_uint(f.o[i][1]),
+                      __float_as_uint(f.o[i][2]), __float_as_uint(f.o[i][3])));
+  const float l0 = quad_sum(f.l[0]), l1 = quad_sum(f.l[1]);
+  sts128(base + 8192 + lane * 16, make_uint4(__float_as_uint(f.m[0]), __float_as_uint(f.m[1]),
+                                             __float_as_uint(l0), __float_as_uint(l1)));
 }
+
+// Two log-sum-exp states of the same two rows, (M, L, a) += (m, l, x) (m in log2 units).
+__device__ __forceinline__ void lse_combine(float &M0, float &M1, float &L0, float &L1, float4 &a,
+                                            float m0, float m1, float l0, float l1, float4 x) {
+  const float n0 = fmaxf(M0, m0), n1 = fmaxf(M1, m1);
+  const float c0 = n0 == -INFINITY ? 0.f : fast_exp2(M0 - n0);
+  const float c1 = n1 == -INFINITY ? 0.f : fast_exp2(M1 - n1);
+  const float w0 = n0 == -INFINITY ? 0.f : fast_exp2(m0 - n0);
+  const float w1 = n1 == -INFINITY ? 0.f : fast_exp2(m1 - n1);
+  a.x = a.x * c0 + x.x * w0;
+  a.y = a.y * c0 + x.y * w0;
+  a.z = a.z * c1 + x.z * w1;
+  a.w = a.w * c1 + x.w * w1;
+  L0 = L0 * c0 + l0 * w0;
+  L1 = L1 * c1 + l1 * w1;
+  M0 = n0;
+  M1 = n1;
+}
+
+// The CTA's last sequence end, all consumer threads at once: the nsl token slices of each
+// of the mt m-tiles (slot s * mt + mtile at base) merged element by element.  whole: the
+// normalised output rows (and lse) of the sequence; otherwise the CTA's partial (m, L and
+// the unnormalised accumulators, fragment order) into workspace slot `slot`.
+template <int KVT>
+__device__ void merge_slots(const KParams &p, uint32_t base, int nsl, int mt, bool whole,
+                            int row0, int head0, int slot, int ctid) {
+  const int units = mt * 512;
+  const int64_t per_slot = (int64_t)(p.mmax / kG) * 512;  // float4s per workspace slot
+  for (int u = ctid; u < units; u += kNCW * 32) {
+    const int mtile = u >> 9, rem = u & 511, i = rem >> 5, ln = rem & 31, g = ln >> 2, t = ln & 3;
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int sl = 0; sl < nsl; ++sl) {
+      const uint32_t sb = base + (sl * mt + mtile) * kSlotBytes;
+      const uint4 a = lds128(sb + 8192 + ln * 16), b = lds128(sb + rem * 16);
+      lse_combine(M0, M1, L0, L1, acc, __uint_as_float(a.x), __uint_as_float(a.y),
+                  __uint_as_float(a.z), __uint_as_float(a.w),
+                  make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z),
+                              __uint_as_float(b.w)));
+    }
+    if (whole) {
+      const float s0 = L0 > 0.f ? p.vpost / L0 : 0.f, s1 = L1 > 0.f ? p.vpost / L1 : 0.f;
+      store_unit<KVT>(p, row0 + mtile, head0, i, g, t, acc, s0, s1);
+      if (i == 0 && t == 0 && p.lse != nullptr) {
+        float *lp = p.lse + (int64_t)(row0 + mtile) * (p.Hkv * kG) + head0 + g;
+        lp[0] = L0 > 0.f ? (M0 + log2f(L0)) * kLn2 : -INFINITY;
+        lp[8] = L1 > 0.f ? (M1 + log2f(L1)) * kLn2 : -INFINITY;
+      }
+    } else {
+      const int64_t ms = (int64_t)slot * (p.mmax / kG) + mtile;
+      __stcg(reinterpret_cast<float4 *>(p.part_o) + (int64_t)slot * per_slot + mtile * 512 + rem, acc);
+      if (i == 0 && t == 0)
+        __stcg(reinterpret_cast<float4 *>(p.part_ml) + ms * 8 + g, make_float4(M0, M1, L0, L1));
+    }
+  }
+}
+
+// One share of a split sequence's merge, once every CTA of the sequence has stored its
+// partial: CTA j of the sequence's nc CTAs merges float4 units [j U / nc, (j + 1) U / nc)
+// of the U = q_len * 512 units of the output, G threads per unit (a power of two; each
+// reads every G-th partial, then the G states combine through shuffles), so that every
+// partial's load is in flight at once.
+template <int KVT>
+__device__ void merge_share(const KParams &p, int h, int row0, int qlen, int c_first, int nc,
+                            int j, int ctid) {
+  constexpr int kBatch = 4;  // partials per thread per memory round trip
+  const int U = qlen * 512;
+  const int u0 = (int)((int64_t)j * U / nc), u1 = (int)((int64_t)(j + 1) * U / nc);
+  const int share = u1 - u0;
+  int G = 1;
+  while (G < 32 && G < nc && share * G * 2 <= kNCW * 32) G <<= 1;
+  const float4 *po = reinterpret_cast<const float4 *>(p.part_o);
+  const float4 *pml = reinterpret_cast<const float4 *>(p.part_ml);
+  const int64_t per_slot = (int64_t)(p.mmax / kG) * 512;
+  for (int q0 = 0; q0 < share * G; q0 += kNCW * 32) {
+    const int q = q0 + ctid, uu = q / G, sub = q & (G - 1);
+    const bool live = uu < share;
+    const int u = u0 + (live ? uu : 0);
+    const int mtile = u >> 9, rem = u & 511, i = rem >> 5, ln = rem & 31, g = ln >> 2, t = ln & 3;
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) {
+      for (int k0 = sub; k0 < nc; k0 += kBatch * G) {
+        float4 ml[kBatch], x[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int k = k0 + b * G;
+          if (k < nc) {
+            const int64_t sl = slot_of(c_first + k, c_first);
+            ml[b] = __ldcg(pml + (sl * (p.mmax / kG) + mtile) * 8 + g);
+            x[b] = __ldcg(po + sl * per_slot + mtile * 512 + rem);
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b)
+          if (k0 + b * G < nc) lse_combine(M0, M1, L0, L1, acc, ml[b].x, ml[b].y, ml[b].z, ml[b].w, x[b]);
+      }
+    }
+    for (int o = 1; o < G; o <<= 1) {  // G | 32: the G threads of a unit sit in one warp
+      const float m0 = __shfl_xor_sync(~0u, M0, o), m1 = __shfl_xor_sync(~0u, M1, o);
+      const float l0 = __shfl_xor_sync(~0u, L0, o), l1 = __shfl_xor_sync(~0u, L1, o);
+      float4 x;
+      x.x = __shfl_xor_sync(~0u, acc.x, o);
+      x.y = __shfl_xor_sync(~0u, acc.y, o);
+      x.z = __shfl_xor_sync(~0u, acc.z, o);
+      x.w = __shfl_xor_sync(~0u, acc.w, o);
+      lse_combine(M0, M1, L0, L1, acc, m0, m1, l0, l1, x);
+    }
+    if (live && sub == 0) {
+      const float s0 = L0 > 0.f ? p.vpost / L0 : 0.f, s1 = L1 > 0.f ? p.vpost / L1 : 0.f;
+      store_unit<KVT>(p, row0 + mtile, h * kG, i, g, t, acc, s0, s1);
+      if (i == 0 && t == 0 && p.lse != nullptr) {
+        float *lp = p.lse + (int64_t)(row0 + mtile) * (p.Hkv * kG) + h * kG + g;
+        lp[0] = L0 > 0.f ? (M0 + log2f(L0)) * kLn2 : -INFINITY;
+        lp[8] = L1 > 0.f ? (M1 + log2f(L1)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+}
+
+
 
 }  // namespace pa

@@ -110,6 +110,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
   locate(tstart, p.num_seqs, p.Hkv, a, rw, hw, tjw);
   int ntw = tstart[rw + 1] - tstart[rw];
   int seg = 0, qlen = 1, row0 = 0, L = 0, mode = 0;  // mode 0: quad, 1: paired, 2: all
+  int f0_cur = 0;  // merge generation of the current sequence (every thread holds it)
   for (int i = 0; i < n; ++i) {
     const int s = i % p.nstage;
     const int r = rw, h = hw, tj = tjw, nt = ntw, gt = a + i;
@@ -127,6 +128,9 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     const bool end = (i == n - 1) || (tj == nt - 1);
     const bool whole = gt - tj >= a && gt - tj + nt <= b;
     bool have = false;
+    // the merge generation of a sequence split across CTAs, read as the sequence begins here
+    // (long before this CTA counts its partial, so the load's latency is hidden)
+    if (begin && !whole) f0_cur = *reinterpret_cast<volatile int32_t *>(p.flags + r * p.Hkv + h);
     if (begin) {
       if (!wait_tile(sm, s, (i / p.nstage) & 1, gt)) {
         if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
@@ -142,7 +146,9 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       mt = qlen;
       paired = mt <= 4;
       // FP8 with one query token: four groups of two warps take every fourth tile, each
-      // warp a 64-token half (two independent chains per step).
+      // warp a 64-token half (eight independent accumulator chains per step).  (All eight
+      // warps on every tile, 16 tokens each, holds a stage for less time but leaves each
+      // warp too little work between its waits: 128K 91.8 against 63.6 us.)
       quad = KVT == PA_KV_FP8_E4M3 && mt == 1;
       if (quad) {
         mode = 0;
@@ -200,7 +206,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
             pos0[hf] = pp < 0 ? -1 : pp + (tk & (p.ps - 1)) + 2 * t;
           }
         }
-        chunk_fp8<SM, 2>(p, st, tb, masked, pos0, cut, L, g, t, f);
+        chunk_fp8<SM, 8>(p, st, tb, masked, pos0, cut, L, g, t, f);
       } else {
         for (int tb = sub * tps; tb < (sub + 1) * tps; tb += 32) {
           int pos0[2] = {0, 0};
@@ -213,7 +219,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
             }
           }
           if (KVT == PA_KV_FP8_E4M3)
-            chunk_fp8<SM, 1>(p, st, tb, masked, pos0, cut, L, g, t, f);
+            chunk_fp8<SM, 4>(p, st, tb, masked, pos0, cut, L, g, t, f);
           else
             chunk_bf16(p, st, tb, masked, pos0, cut, meta->page_pos, L, zero_line(sm), g, t, lane, f);
         }
@@ -227,39 +233,46 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     if (!end) continue;
 
     // ---- end of this CTA's part of sequence (r, h): merge the token slices -----------
-    // Pairs of slices while more than 4 remain, then all remaining into slice 0, so the
-    // exchange buffer (4 slots) is never exceeded: 8 slices take two rounds.
-    for (int cnt = nsl; cnt > 1;) {
-      if (cnt > 4 || (cnt - 1) * mt > 4) {
-        const int half = cnt >> 1;
-        if (active && slice >= half && slice < cnt) put_state(sm, (slice - half) * mt + mtile, f, lane);
-        cons_sync(p, sm, cphase);
-        if (active && slice < half) merge_state(sm, slice * mt + mtile, f, lane);
-        cons_sync(p, sm, cphase);
-        cnt = half;
-      } else {
-        if (active && slice >= 1 && slice < cnt) put_state(sm, (slice - 1) * mt + mtile, f, lane);
-        cons_sync(p, sm, cphase);
-        if (active && slice == 0) merge_states(sm, mtile, cnt - 1, mt, f, lane);
-        cons_sync(p, sm, cphase);
-        cnt = 1;
-      }
-    }
-    const bool writer = active && slice == 0;
-    if (whole) {
-      if (writer) write_final<KVT>(p, f, row0 + mtile, h * kG, g, t);
-      continue;
-    }
-    // A split sequence: store this CTA's partial.  If the sequence ends before the CTA's
-    // last tile it is the one the CTA started in the middle of: its writers count the
-    // arrival at once (the other warps stream on), so that its merge falls to one of
-    // the sequence's other CTAs.  The sequence the CTA leaves unfinished is counted
-    // after the last tile.
+    if (SM == PA_SCALE_PER_TOKEN && active) unfold_rows(f);
     const int gs = tstart[r] * p.Hkv + h * nt;
-    int c_first, nc;
-    seq_ctas(p, tstart, r, h, gs, gs + nt, c_first, nc);
-    if (writer) write_partial(p, f, slot_of(blockIdx.x, c_first), mtile, g, t, lane);
+    int c_first = blockIdx.x, nc = 1;
+    if (!whole) seq_ctas(p, tstart, r, h, gs, gs + nt, c_first, nc);
+    const int slot = slot_of(blockIdx.x, c_first);
     const bool is_head = i < n - 1;
+    // At the CTA's last sequence end no tile is in flight any more: every warp puts its
+    // state into stage memory and all consumer threads merge the slices element by element,
+    // in one step.  Mid-stream ends pair slices through the exchange buffer.
+    const bool in_stage = kSlotMerge && !is_head && nsl > 1 && nsl * mt <= kMaxSlots &&
+                          p.nstage * p.stage_bytes >= kMaxSlots * kSlotBytes;
+    if (in_stage) {
+      cons_sync(p, sm, cphase);  // every warp is done with its tiles
+      if (active) put_slot(sm.stage(0) + (slice * mt + mtile) * kSlotBytes, f, lane);
+      cons_sync(p, sm, cphase);
+      merge_slots<KVT>(p, sm.stage(0), nsl, mt, whole, row0, h * kG, slot, ctid);
+      if (whole) continue;
+    } else {
+      // Rounds of pairs through the exchange buffer: the top mv slices (as many as its
+      // xslots slots hold, all m-tiles each) merge into the mv below them.
+      for (int cnt = nsl; cnt > 1;) {
+        const int mv = min(cnt >> 1, p.xslots / mt), lo = cnt - mv;
+        if (active && slice >= lo && slice < cnt) put_state(sm, (slice - lo) * mt + mtile, f, lane);
+        cons_sync(p, sm, cphase);
+        if (active && slice >= lo - mv && slice < lo)
+          merge_state(sm, (slice - lo + mv) * mt + mtile, f, lane);
+        cons_sync(p, sm, cphase);
+        cnt = lo;
+      }
+      const bool writer = active && slice == 0;
+      if (whole) {
+        if (writer) write_final<KVT>(p, f, row0 + mtile, h * kG, g, t);
+        continue;
+      }
+      // A split sequence: store this CTA's partial.
+      if (writer) write_partial(p, f, slot, mtile, g, t, lane);
+    }
+    // The partial is stored.  If the sequence ends before the CTA's last tile it is the one
+    // the CTA started in the middle of: it is counted at once (the other warps stream on).
+    // The sequence the CTA leaves unfinished is counted after the last tile.
     if (ctid == 0) {
       int32_t *rec = sm.misc() + (is_head ? M_HEAD : M_TAIL);
       rec[0] = r;
@@ -268,17 +281,17 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       rec[3] = qlen;
       rec[4] = c_first;
       rec[5] = nc;
+      sm.misc()[M_F0 + (is_head ? 0 : 1)] = f0_cur;
     }
     if (is_head) {
       has_head = true;
-      if (writer) {
+      if (active && slice == 0) {
         __threadfence();
         if (lane == 0) {
           const int w = atomicAdd(&sm.misc()[M_WCNT], 1);
           if (w == mt - 1) {
             sm.misc()[M_WCNT] = 0;
-            const int old = atomicAdd(p.counters + (r * p.Hkv + h), 1);
-            sm.misc()[M_LAST] = (old == nc - 1) ? 1 : 0;
+            arrive_split(p, sm, r * p.Hkv + h, nc, f0_cur, 0);
           }
         }
       }
@@ -289,24 +302,38 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
 
   if (!(has_head || has_tail)) return;
   if (has_tail) {
-    __threadfence();
+    // every consumer thread's partial stores are ordered before the barrier; the one
+    // thread that counts the partial fences them for the whole CTA
     cons_sync(p, sm, cphase);
     if (ctid == 0) {
       const int32_t *rec = sm.misc() + M_TAIL;
-      const int old = atomicAdd(p.counters + (rec[0] * p.Hkv + rec[1]), 1);
-      sm.misc()[M_LAST + 1] = (old == rec[5] - 1) ? 1 : 0;
+      __threadfence();
+      arrive_split(p, sm, rec[0] * p.Hkv + rec[1], rec[5], f0_cur, 1);
     }
   }
   cons_sync(p, sm, cphase);
 #pragma unroll 1
   for (int k = 0; k < 2; ++k) {
     const bool mine_k = k == 0 ? has_head : has_tail;
-    if (!mine_k || !sm.misc()[M_LAST + k]) continue;
+    if (!mine_k) continue;
     const int32_t *rec = sm.misc() + (k == 0 ? M_HEAD : M_TAIL);
-    const int rr = rec[0], hh = rec[1];
-    __threadfence();
-    merge_partials<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], ctid);
-    if (ctid == 0) p.counters[rr * p.Hkv + hh] = 0;
+    const int hh = rec[1];
+    if (kShareMerge && p.coresident) {
+      // every CTA of the sequence takes a share of its merge once all have arrived
+      if (!sm.misc()[M_LAST + k]) {
+        if (ctid == 0) {
+          const int seq = rec[0] * p.Hkv + hh, f0 = sm.misc()[M_F0 + k];
+          if (!wait_flag(p.flags + seq, f0)) raise_flag(p, sm, PA_DEV_TIMEOUT);
+          __threadfence();
+        }
+        cons_sync(p, sm, cphase);
+      }
+      merge_share<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], (int)blockIdx.x - rec[4], ctid);
+    } else if (sm.misc()[M_LAST + k]) {
+      // CTAs of one sequence may run in different waves: the last to arrive merges alone
+      __threadfence();
+      merge_partials<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], ctid);
+    }
   }
 }
 

@@ -13,6 +13,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_fp16.h>
 
@@ -28,6 +29,7 @@ constexpr int kQRow = 144;          // halves per staged query row (72 words)
 constexpr int kMaxRowHeads = 16;    // q_len * index_heads of one request
 constexpr int kMaxStride = 16384;   // pages per row the selection sorts
 constexpr int kMaxTopk = 1024;
+constexpr int kMaxDevices = 64;     // devices whose selection-kernel opt-in is tracked
 
 struct IdxParams {
   const uint16_t *q;
@@ -337,21 +339,28 @@ extern "C" pa_status_t pa_index_topk(const pa_index_args_t *a, void *stream) {
   p.cscale = a->sm_scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int gx = (a->block_table_stride + kWarps * kPagesPerWarp - 1) / (kWarps * kPagesPerWarp);
-  index_score_kernel<<<dim3(gx, p.B), kWarps * 32, 0, s>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   int n = 1;
   while (n < a->block_table_stride) n <<= 1;
   const size_t smem = (size_t)n * sizeof(unsigned long long);
   if (smem > 48 * 1024) {
-    static bool opted = false;  // the kernel's opt-in limit, set once
-    if (!opted) {
-      if (cudaFuncSetAttribute(index_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(kMaxStride * sizeof(unsigned long long))) != cudaSuccess)
-        return PA_ERR_CUDA;
-      opted = true;
-    }
+    // the selection kernel's opt-in shared-memory limit, set once per device (the
+    // attribute belongs to the device's context)
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t opt_err[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    std::call_once(once[dev], [dev]() {
+      opt_err[dev] = cudaFuncSetAttribute(index_select_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)(kMaxStride * sizeof(unsigned long long)));
+    });
+    if (opt_err[dev] != cudaSuccess) return PA_ERR_CUDA;
   }
+  const int gx = (a->block_table_stride + kWarps * kPagesPerWarp - 1) / (kWarps * kPagesPerWarp);
+  (void)cudaGetLastError();  // drop an earlier, unrelated launch error
+  index_score_kernel<<<dim3(gx, p.B), kWarps * 32, 0, s>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   const int threads = n >= 2048 ? 1024 : (n >= 64 ? n / 2 : 32);
   index_select_kernel<<<a->num_rows, threads, smem, s>>>(p, n);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -44,8 +44,12 @@ constexpr int kLaunchRegs = 168, kProdRegs = 56, kConsRegs = 224;
 static_assert(kNCW * 32 * kConsRegs + 4 * 32 * kProdRegs == kThreads * kLaunchRegs,
               "register split must match the launch allocation");
 constexpr int kMaxQ = 8;         // most query tokens per request (m-tiles)
+// End of a CTA's last sequence: its token slices merge in stage memory in one step (true)
+// or pair through the exchange buffer (false).  A sequence split across co-resident CTAs:
+// every one of them merges a share of it (true), or the last to arrive merges it (false).
+constexpr bool kSlotMerge = true, kShareMerge = true;
 constexpr int kQRowBytes = kG * kD * 2;   // one query token's 16 heads, bf16
-constexpr int kMergeBytes = 4 * 8192 + 4 * 512;
+constexpr int kMergeBytes = 4 * 8192 + 4 * 512;  // the exchange buffer at 4 slots
 constexpr int kUmmaBars = 24;    // extra mbarriers of the tcgen05 kernel
 constexpr int kDumpHeader = 128;
 constexpr float kLn2 = 0.693147180559945309f;
@@ -73,17 +77,23 @@ struct KParams {
   float *lse;
   uint32_t *status;
   int32_t *counters;              // [num_seqs * Hkv] arrivals of split-K partials
+  int32_t *flags;                 // [num_seqs * Hkv] generation of each sequence's merge (bumped by
+                                  // the last arrival; the other CTAs wait for the bump)
   float *part_ml;                 // [slots][2][mmax]  (m in log2 units, l)
   float *part_o;                  // [slots][mmax][128] (unnormalised)
   uint8_t *dump;
   int64_t dump_tiles;
   int64_t num_pages;
   float kfold;                    // score = acc * kfold (* k_scale[token] in per-token mode)
-  float pfold;                    // P' = p * v_scale[token] * pfold (per-token mode)
+  float pfold;                    // unused (1): the per-token V scale's power of two is per warp
   float vpost;                    // out = (o / l) * vpost
   int32_t num_seqs, Hkv, ps, ps_shift, ppt, bt_stride, sel_stride, q_uniform, max_q, max_ctx;
   int32_t num_rows, out_f32, sched_partition, part_tiles, maxch, grid, nstage, mmax, sparse;
   int32_t off_q, qslot_bytes, off_merge, off_tstart, off_meta, off_bar, off_misc, stage_bytes;
+  int32_t xslots;                 // slots of the exchange buffer (4, or 2 for one-token FP8 plans)
+  int32_t coresident;             // every CTA of the grid is resident at once (one per SM): the
+                                  // CTAs of a split sequence may wait for each other and share
+                                  // its merge; otherwise the last arrival merges it alone
 };
 
 // ------------------------------------------------------------------ per-request geometry
@@ -401,7 +411,7 @@ __device__ __forceinline__ int slot_of(int c, int c_first) { return c == c_first
 struct Smem {
   uint8_t *base;           // generic pointer to the 1024-aligned base
   uint32_t sb;             // its shared-window address
-  uint32_t stage_bytes, nstage, q0, qslot_bytes, merge_a, bar0;
+  uint32_t stage_bytes, nstage, q0, qslot_bytes, merge_a, merge_ml, bar0;
   int32_t *tstart_p, *misc_p;
   StageMeta *meta_p;
   __device__ static Smem make(uint8_t *b, const KParams &p) {
@@ -413,6 +423,7 @@ struct Smem {
     m.q0 = m.sb + p.off_q;
     m.qslot_bytes = p.qslot_bytes;
     m.merge_a = m.sb + p.off_merge;
+    m.merge_ml = m.merge_a + p.xslots * 8192;
     m.bar0 = m.sb + p.off_bar;
     m.tstart_p = reinterpret_cast<int32_t *>(b + p.off_tstart);
     m.misc_p = reinterpret_cast<int32_t *>(b + p.off_misc);
@@ -422,6 +433,7 @@ struct Smem {
   __device__ uint32_t stage(int s) const { return sb + s * stage_bytes; }
   __device__ uint32_t qslot(int k) const { return q0 + k * qslot_bytes; }
   __device__ uint32_t merge() const { return merge_a; }
+  __device__ uint32_t merge_ml_at(int k) const { return merge_ml + k * 512; }
   __device__ int32_t *tstart() const { return tstart_p; }
   __device__ StageMeta *meta(int s) const { return meta_p + s; }
   __device__ uint32_t full(int s) const { return bar0 + 8 * s; }
@@ -438,9 +450,10 @@ struct Smem {
 // M_TMEM: TMEM base address of the tcgen05 kernel.  M_ZERO: a 16-byte line of zeros.
 // M_QHDR: (request, KV head, q_len, first row, context) of the request whose query sits
 // in query slot k, at M_QHDR + 8 k; written by the producer with the request's first tile.
+// M_F0, M_F0 + 1: the merge generation of the head / tail sequence read before arriving.
 enum : int {
   M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24, M_TMEM = 30,
-  M_ZERO = 32, M_QHDR = 40
+  M_ZERO = 32, M_QHDR = 40, M_F0 = 56
 };
 constexpr int kMiscBytes = 256;
 
@@ -453,6 +466,36 @@ __device__ __forceinline__ bool wait_tile(const Smem &sm, int s, uint32_t parity
   const long long t0 = clock64();
   while (!(mbar_try_wait(sm.full(s), parity) && *id == gt)) {
     if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
+// Counts this CTA's partial of split sequence `seq` (nc CTAs): one thread, after the
+// partial's stores are fenced.  f0 is the sequence's merge generation, read when the
+// sequence began in this CTA (before any arrival of this call can have bumped it).  The
+// last CTA to arrive resets the arrival counter (all have arrived) and bumps the
+// generation, which releases the CTAs that wait for it.  misc[M_LAST + k] says whether this
+// CTA was the last (k: 0 head, 1 tail).
+__device__ __forceinline__ void arrive_split(const KParams &p, const Smem &sm, int seq, int nc,
+                                             int f0, int k) {
+  const int old = atomicAdd(p.counters + seq, 1);
+  const bool last = old == nc - 1;
+  if (last) {
+    __threadfence();  // the other CTAs' partials (fenced before their arrivals) are visible
+    *reinterpret_cast<volatile int32_t *>(p.counters + seq) = 0;
+    *reinterpret_cast<volatile int32_t *>(p.flags + seq) = f0 + 1;
+  }
+  sm.misc()[M_LAST + k] = last ? 1 : 0;
+}
+
+// Waits (bounded) until the merge generation at `flag` differs from f0.  False on timeout.
+__device__ __forceinline__ bool wait_flag(const int32_t *flag, int f0) {
+  const volatile int32_t *v = flag;
+  if (*v != f0) return true;
+  const long long t0 = clock64();
+  while (*v == f0) {
+    if (clock64() - t0 > kWaitCycles) return false;
+    __nanosleep(64);
   }
   return true;
 }

@@ -51,6 +51,55 @@ __device__ __forceinline__ uint4 load_nc16(const void *p) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Codes of x[d] / s for 16 values: the e4m3 rounding (to nearest, ties to even, saturating
+// at 448) of the exact quotient, s = fl(amax / 448) the stored scale.  Why one product is
+// enough: with T = 448 x / amax (x, amax bf16: 8 significant bits each), 448 x - m amax is a
+// multiple of a power of two for every rounding midpoint m (5 significant bits), so T is
+// either exactly a midpoint or at least 2^-13 (relative) away from all of them; and x / s
+// = T (amax / 448) / s lies within 2^-24 of T.  So a q within 2^-19 of x / s rounds like it,
+// except where T is a midpoint: there x / s sits just below it when s was rounded up, just
+// above when s was rounded down, and on it when s is exact -- the sign of 448 s - amax, one
+// fma per row.  Hence q = x * A + x * B with, per row, r = 1/s rounded to nearest and
+//   s rounded up or down: A = r (1 -+ 2^-20), B = 0: the bias pushes ties to the right side;
+//   s exact: A = r, B = (1 - s r) r, the part of 1/s that r misses, so that q is x / s to
+//     2^-47 and a tie lands on the midpoint itself, which the conversion rounds to even.
+// Signs need nothing: the bias is relative and the conversion is symmetric.
+__device__ __forceinline__ void encode_with(const float (&x)[16], float A, float B, float xs,
+                                            uint32_t (&c)[4]) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a = x[4 * w + k] * xs;
+      q[k] = fmaf(a, A, a * B);
+    }
+    c[w] = pack4_e4m3(q[0], q[1], q[2], q[3]);
+  }
+}
+
+__device__ __forceinline__ void encode_scaled(const float (&x)[16], float amax, float s, float xs,
+                                              uint32_t (&c)[4]) {
+  const float r = __frcp_rn(s);
+  const float side = fmaf(s, kE4m3Max, -amax);  // its sign is exact: 448 s - amax
+  float A = r, B = 0.f;
+  if (side > 0.f)
+    A = r * (1.f - 0x1p-20f);
+  else if (side < 0.f)
+    A = r * (1.f + 0x1p-20f);
+  else
+    B = fmaf(-s, r, 1.f) * r;
+  encode_with(x, A, B, xs, c);
+}
+
+__device__ __forceinline__ void encode_row(const float (&x)[16], float amax, float scale,
+                                           uint32_t (&c)[4]) {
+  if (scale < 0x1p-100f)  // keep 1 / s finite: x, amax and s times 2^100, exactly
+    encode_scaled(x, amax * 0x1p100f, scale * 0x1p100f, 0x1p100f, c);
+  else
+    encode_scaled(x, amax, scale, 1.f, c);
+}
+
 // One warp step covers kUnits (token, KV head) units, i.e. 2 kUnits rows (K and V).  Lane
 // octet o (lanes 8o .. 8o+7) takes rows o, o + 4, ...: row r is unit r / 2, K if r is even,
 // and each lane holds 16 of the row's values (32 bytes).
@@ -104,24 +153,14 @@ __device__ __forceinline__ void quantize_step(const KvWriteParams &p, const Step
     for (int d = 0; d < 16; ++d) amax = fmaxf(amax, fabsf(x[d]));
 #pragma unroll
     for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    // scale = amax / 448 is stored; the codes use the fp32 reciprocal 448 / amax (the
-    // quotient x / scale where that reciprocal overflows: amax below about 1.3e-36).
+    // scale = amax / 448, rounded once to fp32, is stored; each code is the e4m3 rounding
+    // of the exact quotient x / scale.
     const float scale = __fdiv_rn(amax, kE4m3Max);
     uint4 codes = make_uint4(0, 0, 0, 0);
-    if (amax != 0.f) {
-      const float inv = __fdiv_rn(kE4m3Max, amax);
-      float q[16];
-      if (!isinf(inv)) {
-#pragma unroll
-        for (int d = 0; d < 16; ++d) q[d] = __fmul_rn(x[d], inv);
-      } else {
-#pragma unroll
-        for (int d = 0; d < 16; ++d) q[d] = __fdiv_rn(x[d], scale);
-      }
-      codes.x = pack4_e4m3(q[0], q[1], q[2], q[3]);
-      codes.y = pack4_e4m3(q[4], q[5], q[6], q[7]);
-      codes.z = pack4_e4m3(q[8], q[9], q[10], q[11]);
-      codes.w = pack4_e4m3(q[12], q[13], q[14], q[15]);
+    if (scale != 0.f) {
+      uint32_t c[4];
+      encode_row(x, amax, scale, c);
+      codes = make_uint4(c[0], c[1], c[2], c[3]);
     }
     if (!live) continue;
     const int head = p.Hkv == 1 ? 0 : u % p.Hkv;
@@ -227,6 +266,7 @@ extern "C" pa_status_t pa_kv_quantize_write(const pa_kv_write_args_t *a, void *s
   const int64_t want = (groups + kWarps - 1) / kWarps;
   const int64_t cap = (int64_t)sms * (per_sm > 0 ? per_sm : 1);  // one wave of resident CTAs
   const int grid = (int)(want < cap ? want : cap);
+  (void)cudaGetLastError();  // drop an earlier, unrelated launch error
   kv_quantize_write_kernel<kPipe><<<grid, kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

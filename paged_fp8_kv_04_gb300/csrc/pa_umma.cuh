@@ -12,17 +12,17 @@
 //                                        per (warp slice, head) by warp reduction, exp2.
 //   O_w^T[d][n] = V^T[d][tok] . P^T      kind::f8f6f4 again, M = 128 head_dim lanes, N = 16,
 //                                        A = the V tile as TMA left it (MN-major), B = P as
-//                                        e4m3 hi + lo relative to the slice's tile maximum
-//                                        with the per-token V scale folded in; one O tile
-//                                        per 32-token slice.
+//                                        e4m3 hi + lo with the per-token V scale folded in,
+//                                        relative to the slice's largest p * v_scale per
+//                                        head; one O tile per 32-token slice.
 //   O update                             TMEM lane = head_dim: o = o * alpha + O_w * beta in
 //                                        fp32 registers, one tile late so that it overlaps
 //                                        the next tile's softmax and the PV in flight.
 // Neither K nor V is widened on the SM sub-partitions; the tensor core reads the cache
-// bytes.  P is carried with 8 significant bits (hi + lo) relative to the maximum of its
-// own 32 tokens, so a tile's small probabilities are not flushed however far below the
-// running maximum the tile lies; what a tile can lose is below 2^-18 of its largest
-// weight per token.
+// bytes.  P is carried with 8 significant bits (hi + lo) relative to the largest
+// p * v_scale of its own 32 tokens, so a tile's small probabilities are not flushed however
+// far below the running maximum the tile lies, nor a token's weight by a neighbour's
+// larger V scale; what a tile can lose is below 2^-18 of its largest weighted term.
 //
 // Warp roles (384 threads): warps 0-7 run the softmax on every tile (warp w: token slice
 // w & 3, heads 8 (w >> 2) .. + 7); warp 8 is the TMA producer (the same page gather as the
@@ -444,19 +444,35 @@ __device__ void run_softmax(const KParams &p, const Smem &sm, const UBars &ub, i
       mr[k] = mn;
       x[k] = fast_exp2(x[k] - (tmx == -INFINITY ? 0.f : tmx));  // p relative to the tile max
     }
-    float W = 1.f, wf = 256.f;
-    if (SM == PA_SCALE_PER_TOKEN) {
-      W = warp_max_f32(vs);
-      wf = W > 0.f ? vs * __frcp_rn(W) * 256.f : 0.f;
+    // per head, W = the slice's largest p * v_scale: the largest product, not the largest
+    // scale, so that a token with p = 1 and a small scale keeps its 8 bits next to a token
+    // with a large scale and p ~ 0
+    // with a power of two F = 2^(7 - floor(log2 W)) (at most 2^120): P' = p * v_scale * F
+    // <= 256, and the O tile is scaled back by 1 / F
+    float xv[8], F[8], Fi[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (SM == PA_SCALE_PER_TOKEN) {
+        xv[k] = x[k] * vs;
+        const float W = warp_max_f32(xv[k]);
+        const int ew = (int)((__float_as_uint(W) >> 23) & 0xFFu) - 127;
+        const int ef = min(7 - ew, 120);
+        F[k] = W > 0.f ? __uint_as_float((uint32_t)(ef + 127) << 23) : 0.f;
+        Fi[k] = W > 0.f ? __uint_as_float((uint32_t)(127 - ef) << 23) : 0.f;
+      } else {
+        xv[k] = x[k];
+        F[k] = 256.f;
+        Fi[k] = 1.f / 256.f;
+      }
     }
-    // ---- P' = p * (v_scale / W) * 256 as e4m3 hi + lo; running sums
+    // ---- P' = p * v_scale * F as e4m3 hi + lo; running sums
     uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int k0 = 2 * j, k1 = 2 * j + 1;
       l[k0] = fmaf(l[k0], alpha[k0], x[k0] * gam[k0]);
       l[k1] = fmaf(l[k1], alpha[k1], x[k1] * gam[k1]);
-      const float y0 = x[k0] * wf, y1 = x[k1] * wf;
+      const float y0 = xv[k0] * F[k0], y1 = xv[k1] * F[k1];
       uint32_t c0, c1;
       const float h0 = hi_e4m3(y0, c0), h1 = hi_e4m3(y1, c1);
       hw[j >> 1] |= (c0 | (c1 << 8)) << (16 * (j & 1));
@@ -479,13 +495,12 @@ __device__ void run_softmax(const KParams &p, const Smem &sm, const UBars &ub, i
     sts64(pt, hw[0], hw[1]);
     sts64(pt + 2048, lw[0], lw[1]);
     {  // alpha (rescale of the slice's o) and beta (scale of its new O tile) per head
-      const float bsc = (SM == PA_SCALE_PER_TOKEN ? W : 1.f) * (1.f / 256.f);
       const uint32_t ab = ua + kUAB + (i % 3) * 256 + 64 * q + 32 * hh;
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         if (lane == k) {
           sts_f32(ab + 4 * k, alpha[k]);
-          sts_f32(ab + 768 + 4 * k, gam[k] * bsc);
+          sts_f32(ab + 768 + 4 * k, gam[k] * Fi[k]);
         }
     }
     if (masked && hh == 0) {  // a masked slot's V bytes may be stale or NaN codes: 0 * NaN = NaN

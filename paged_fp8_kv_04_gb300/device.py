@@ -35,16 +35,18 @@ def to_device(p, device="cuda") -> dict:
 
 
 def plan_for(p, *, out_dtype="bf16", partition_tokens=0, ragged=None, device="cuda",
-             max_context_len=None, q_len=None, **kw) -> Plan:
+             max_context_len=None, q_len=None, max_selected_pages=None, **kw) -> Plan:
     """A plan sized exactly for problem p (its capacity bucket)."""
     rag = ragged if ragged is not None else (p.uniform_q_len is None)
     ql = q_len if q_len is not None else (p.max_q_len if rag else int(p.uniform_q_len))
+    if max_selected_pages is None:
+        max_selected_pages = 0 if p.selected is None else p.selected.shape[1]
     return Plan(device=device, num_kv_heads=p.num_kv_heads, group_size=p.group_size,
                 head_dim=p.head_dim, page_size=p.page_size, kv_dtype=p.kv_dtype,
                 scale_mode=p.scale_mode, q_mode="ragged" if rag else "uniform",
                 q_len=max(ql, 1), max_batch=max(p.num_seqs, 1), max_rows=max(p.num_rows, 1),
                 max_context_len=max_context_len or max(int(p.context_lens.max()), 1),
-                max_selected_pages=0 if p.selected is None else p.selected.shape[1],
+                max_selected_pages=max_selected_pages,
                 partition_tokens=partition_tokens, out_dtype=out_dtype, **kw)
 
 

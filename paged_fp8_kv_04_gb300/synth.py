@@ -116,12 +116,17 @@ def _normal(rng: np.random.Generator, shape) -> np.ndarray:
 
 
 def _fill_pages(rng, pages: np.ndarray, Hkv, ps, D, scale_mode, kv_dtype, k_out, v_out,
-                ks_out, vs_out, kss, vss, chunk=1024):
-    """Draw N(0,1) K/V for the listed physical pages and store their encoding."""
+                ks_out, vs_out, kss, vss, chunk=1024, kv_mag_log2=0.0):
+    """Draw N(0,1) K/V for the listed physical pages and store their encoding.  With
+    kv_mag_log2 = M > 0 every (page, KV head, slot) row is first multiplied by its own
+    2^u, u uniform in [-M, M] (K and V drawn independently)."""
     for i in range(0, len(pages), chunk):
         idx = pages[i:i + chunk]
         for which, out, sout, ss in ((0, k_out, ks_out, kss), (1, v_out, vs_out, vss)):
             x = _normal(rng, (len(idx), Hkv, ps, D))
+            if kv_mag_log2 > 0:
+                u = rng.uniform(-kv_mag_log2, kv_mag_log2, size=(len(idx), Hkv, ps, 1))
+                x = (x * np.exp2(u)).astype(np.float32)
             if scale_mode == "per_token":
                 codes, sc = quantize_per_token(x)
             elif scale_mode == "scalar":
@@ -146,9 +151,12 @@ def make_problem(seed: int, *, num_seqs: int, context_lens: Sequence[int],
                  head_dim: int = 128, page_size: int = 128, kv_dtype: str = "fp8",
                  scale_mode: str = "per_token", pool_pages: Optional[int] = None,
                  selected_pages: Optional[int] = None, block_table_pad: int = 0,
-                 only_selected_data: bool = False, name: str = "") -> Problem:
+                 only_selected_data: bool = False, kv_mag_log2: float = 0.0,
+                 q_mag_log2: float = 0.0, name: str = "") -> Problem:
     """General seeded problem.  kv_dtype "bf16" with scale_mode "none" draws bf16 values
-    directly; "bf16" with another scale_mode stores the dequantised e4m3 values."""
+    directly; "bf16" with another scale_mode stores the dequantised e4m3 values.
+    kv_mag_log2 = M gives every K and V token row its own magnitude 2^u, u uniform in
+    [-M, M], before quantisation; q_mag_log2 = Mq does the same for every query element."""
     rng = np.random.default_rng(seed)
     B, Hkv, g, D, ps = num_seqs, num_kv_heads, group_size, head_dim, page_size
     L = np.asarray(context_lens, dtype=np.int64)
@@ -196,10 +204,13 @@ def make_problem(seed: int, *, num_seqs: int, context_lens: Sequence[int],
         used = np.arange(P, dtype=np.int64)
     used = np.asarray(used, dtype=np.int64)
     _fill_pages(rng, used, Hkv, ps, D, scale_mode, kv_dtype, k_cache, v_cache,
-                k_scale, v_scale, kss, vss)
+                k_scale, v_scale, kss, vss, kv_mag_log2=kv_mag_log2)
 
     rows = int(ql.sum())
-    q = bf16_bits(_normal(rng, (rows, Hkv * g, D)))
+    qf = _normal(rng, (rows, Hkv * g, D))
+    if q_mag_log2 > 0:
+        qf = (qf * np.exp2(rng.uniform(-q_mag_log2, q_mag_log2, size=qf.shape))).astype(np.float32)
+    q = bf16_bits(qf)
     cu = np.zeros(B + 1, dtype=np.int32)
     cu[1:] = np.cumsum(ql)
     uni = int(ql[0]) if B and np.all(ql == ql[0]) else None
@@ -212,6 +223,26 @@ def make_problem(seed: int, *, num_seqs: int, context_lens: Sequence[int],
                    block_table=bt, context_lens=L.astype(np.int32), cu_seqlens_q=cu,
                    uniform_q_len=uni, selected=sel, num_selected=nsel,
                    sm_scale=1.0 / float(np.sqrt(D)), name=name)
+
+
+def subset(p: Problem, idx) -> Problem:
+    """The same problem restricted to requests idx (caches and block tables shared)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    ql = p.q_lens[idx]
+    cu = np.zeros(len(idx) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(ql)
+    rows = rows_of(p, idx) if len(idx) else np.zeros(0, np.int64)
+    uni = int(ql[0]) if len(idx) and np.all(ql == ql[0]) else None
+    return dataclasses.replace(
+        p, num_seqs=len(idx), q=p.q[rows], block_table=p.block_table[idx],
+        context_lens=p.context_lens[idx], cu_seqlens_q=cu, uniform_q_len=uni,
+        selected=None if p.selected is None else p.selected[idx],
+        num_selected=None if p.num_selected is None else p.num_selected[idx])
+
+
+def rows_of(p: Problem, idx) -> np.ndarray:
+    """The query rows of requests idx, in order."""
+    return np.concatenate([np.arange(p.cu_seqlens_q[r], p.cu_seqlens_q[r + 1]) for r in idx])
 
 
 # --------------------------------------------------------------------- named workloads
@@ -381,6 +412,8 @@ class KvWriteCase:
     k_scale: np.ndarray           # fp32 [P, Hkv, ps]
     v_scale: np.ndarray
     name: str = ""
+    block_table: Optional[np.ndarray] = None   # int32 [B, pages]: where a prefill layout put each sequence
+    context_lens: Optional[np.ndarray] = None  # int32 [B]
 
 
 def kv_write_case(seed: int, num_tokens: int, num_kv_heads: int = 1, page_size: int = 128,
@@ -432,6 +465,8 @@ def kv_write_prefill_8k(seed: int = 5) -> KvWriteCase:
     pages = rng.permutation(2048).astype(np.int64).reshape(32, 64)
     pos = np.arange(8192, dtype=np.int64)
     c.slot_mapping = (pages[:, pos // 128] * 128 + pos % 128).reshape(-1)
+    c.block_table = pages.astype(np.int32)
+    c.context_lens = np.full(32, 8192, dtype=np.int32)
     return c
 
 

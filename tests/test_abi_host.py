@@ -102,10 +102,14 @@ def test_shared_memory_budget_pinned(lib):
     pinned here (ROCm/ATOM PR 2710 review, "Smaller": an unpinned mirrored LDS budget)."""
     inf = _info(lib, desc())
     assert inf.threads_per_cta == 384 and inf.tile_tokens == 128
-    assert inf.stages == 5 and inf.smem_bytes <= 232448
+    # one query token: a 2-slot exchange buffer (the CTA's last merge runs in stage
+    # memory) leaves room for 6 FP8 stages of 33 KB, 3 BF16 stages of 64 KB
+    assert inf.stages == 6 and inf.smem_bytes <= 232448
     assert inf.grid_ctas == 152 and inf.partial_slots == 304
     bf = _info(lib, desc(kv_dtype="bf16", scale_mode="none"))
-    assert bf.stages == 2 and bf.smem_bytes <= 232448
+    assert bf.stages == 3 and bf.smem_bytes <= 232448
+    q4 = _info(lib, desc(q_len=4, q_mode="ragged", max_batch=64))
+    assert q4.stages == 4 and q4.smem_bytes <= 232448
     q8 = _info(lib, desc(q_len=8, q_mode="ragged", max_batch=4096))
     assert q8.stages >= 2 and q8.smem_bytes <= 232448
 

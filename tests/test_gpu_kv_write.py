@@ -1,8 +1,9 @@
 """The KV quantise-and-write kernel against the oracle, through the C ABI (needs a GPU).
 
-Codes and scales are integer / bit results decided in fp32 on both sides, so the bar is
-bit-exact: every byte of both caches and every scale bit, including the rows the call
-must leave alone.  Then the producer-to-consumer round trip: pa_decode over a cache that
+Codes and scales are integer / bit results (the fp32 scale amax / 448, and each code the
+e4m3 rounding of the exact quotient x / scale on both sides), so the bar is bit-exact:
+every byte of both caches and every scale bit, including the rows the call must leave
+alone.  Then the producer-to-consumer round trip: pa_decode over a cache that
 pa_kv_quantize_write filled equals the oracle's attention over the oracle's cache.
 """
 import numpy as np
@@ -75,6 +76,57 @@ def test_kv_quantize_write_bit_exact(T, Hkv, ps, P, skip, past):
 def test_kv_quantize_write_full_size():
     """The bench's workload (the dense-8K batch written at once), every byte compared."""
     assert_bit_exact(synth.kv_write_prefill_8k(5))
+
+
+def test_kv_quantize_write_near_ties_bit_exact():
+    """Rows whose quotients x / scale sit a hair off an e4m3 rounding midpoint (where an
+    fp32 product with 448 / amax, or an fp32 quotient, would pick the other code): every
+    code as the oracle's exact quotient decides it."""
+    import oracle_pins
+    rows = {}
+    for amax, x in oracle_pins._near_tie_rows():
+        rows.setdefault(amax, []).append(x)
+    xs = np.zeros((len(rows), 2, 128), np.float32)
+    for t, (amax, items) in enumerate(sorted(rows.items())):
+        for d, x in enumerate(items[:127]):
+            xs[t, 0, d] = float(x) * (-1.0 if d % 3 == 1 else 1.0)
+            xs[t, 1, 127 - d] = float(x) * 2.0 ** (-60 + 10 * (t % 13))  # other binades
+        xs[t, 0, 127] = float(amax)
+        xs[t, 1, 0] = float(amax) * 2.0 ** (-60 + 10 * (t % 13))
+    k = synth.bf16_bits(xs)
+    v = synth.bf16_bits(xs[::-1].copy())
+    T, P, ps = xs.shape[0], (xs.shape[0] + 15) // 16, 16
+    c = synth.KvWriteCase(k, v, np.arange(T, dtype=np.int64),
+                          np.full((P, 2, ps, 128), 0x11, np.uint8), np.full((P, 2, ps, 128), 0x22, np.uint8),
+                          np.zeros((P, 2, ps), np.float32), np.zeros((P, 2, ps), np.float32),
+                          name="near ties")
+    assert_bit_exact(c)
+
+
+def test_decode_of_the_written_full_size_cache():
+    """The producer-to-consumer test at full size: the 262144-token batch (per-token
+    magnitudes 2^-20 .. 2^20, zero rows, single-value rows) written by
+    pa_kv_quantize_write, then decoded as the dense-8K batch by pa_decode; every row
+    against the oracle's attention over the oracle's own cache."""
+    import dataclasses
+    c = synth.kv_write_prefill_8k(5)
+    gk, gv, gks, gvs, status = run_gpu(c)
+    ok, ov, oks, ovs, bad = run_oracle(c)
+    assert status == 0 and bad == 0
+    assert np.array_equal(gk, ok) and np.array_equal(gv, ov)
+    base = synth.dense_8k(1)
+    p_gpu = dataclasses.replace(base, k_cache=gk, v_cache=gv, k_scale=gks, v_scale=gvs,
+                                block_table=c.block_table, context_lens=c.context_lens)
+    p_ora = dataclasses.replace(p_gpu, k_cache=ok, v_cache=ov, k_scale=oks, v_scale=ovs)
+    d = dv.to_device(p_gpu)
+    plan = dv.plan_for(p_gpu)
+    out, lse = dv.run(plan, p_gpu, d, lse=True)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    ref, ref_lse = O.decode(p_ora)
+    compare(out.float().cpu().numpy(), ref, "decode of the written cache", rel_rows=True)
+    # scores reach ~1e6 with keys of 2^20: lse to fp32's relative precision
+    compare_lse(lse.cpu().numpy(), ref_lse, "decode of the written cache", rel=1e-5)
 
 
 def test_zero_tokens_is_a_no_op():
