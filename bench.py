@@ -64,7 +64,15 @@ def parse():
 # from one ncu capture per workload, valid only for the kernel sources they were taken on
 # (sha256 over the code, comments stripped, of the C header and the decode kernels'
 # translation unit); any other code gives traffic null.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    "long128k": {"bytes": 279804928, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+    "long128k_scalar": {"bytes": 271451392, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+    "dense8k": {"bytes": 69855232, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+    "bf16ctl": {"bytes": 137147648, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+    "ragged": {"bytes": 143990784, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+    "sparse": {"bytes": 70664448, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+    "prefill": {"bytes": 11231232, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+}
 
 
 def _code_text(path):
@@ -93,7 +101,19 @@ def csrc_sha256():
 
 
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
-MEASURED_TRAFFIC_KV_WRITE = {"bytes": None, "src_sha256": ""}
+# The indexer's two launches of one call (score + select), from the same kind of capture.
+MEASURED_TRAFFIC_INDEXER = {"bytes": 556972800, "src_sha256": "be874bcee95dbc254a2928240b2d519670ef674cbc7b3e9b0900f6b6b28592f0"}
+MEASURED_TRAFFIC_KV_WRITE = {"bytes": 171386368, "src_sha256": "c0729fd8a04a448779a9dd040359180d545aa1e7f4dfb1cf5afe0cdbaae6cb6f"}
+
+
+def index_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for f in (os.path.join(ROOT, "include", "pa.h"),
+              os.path.join(ROOT, "paged_fp8_kv_04_gb300", "csrc", "pa_index.cu")):
+        h.update(os.path.basename(f).encode())
+        h.update(_code_text(f))
+    return h.hexdigest()
 
 
 def kv_write_sha256():
@@ -478,7 +498,7 @@ def _prefill_roofline(p, us_per_call):
     tf = flops / (us_per_call * 1e-6) / 1e12
     tpeak = tensor_peak()
     return {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
-            "frac": tf / tpeak, "traffic": None,
+            "frac": tf / tpeak, "traffic": measured_traffic("prefill"),
             "peak_kind": "measured bf16_tflops (cuBLAS burst); f16 mma.sync runs below it"}
 
 
@@ -735,7 +755,9 @@ def bench_indexer(args, dev, rank, world, local):
         "us_per_call_graph": us, "rows_per_s": R / (us * 1e-6),
         "algorithmic_bytes_per_call": int(total),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": (MEASURED_TRAFFIC_INDEXER["bytes"]
+                                 if MEASURED_TRAFFIC_INDEXER["src_sha256"] == index_sha256() else None),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)"},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * K, "clocks": clk,
     }

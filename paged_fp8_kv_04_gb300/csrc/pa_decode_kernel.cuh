@@ -237,7 +237,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     const int gs = tstart[r] * p.Hkv + h * nt;
     int c_first = blockIdx.x, nc = 1;
     if (!whole) seq_ctas(p, tstart, r, h, gs, gs + nt, c_first, nc);
-    const int slot = slot_of(blockIdx.x, c_first);
+    const int slot = slot_of(sm.misc()[M_VCTA], c_first);
     const bool is_head = i < n - 1;
     // At the CTA's last sequence end no tile is in flight any more: every warp puts its
     // state into stage memory and all consumer threads merge the slices element by element,
@@ -328,7 +328,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
         }
         cons_sync(p, sm, cphase);
       }
-      merge_share<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], (int)blockIdx.x - rec[4], ctid);
+      merge_share<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], sm.misc()[M_VCTA] - rec[4], ctid);
     } else if (sm.misc()[M_LAST + k]) {
       // CTAs of one sequence may run in different waves: the last to arrive merges alone
       __threadfence();

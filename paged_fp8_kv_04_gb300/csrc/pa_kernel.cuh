@@ -96,6 +96,21 @@ struct KParams {
                                   // its merge; otherwise the last arrival merges it alone
 };
 
+// misc[] words
+// M_LAST, M_LAST + 1: merge duty for the head / tail sequence; M_WCNT: writer warps that
+// have stored their part of the head partial; M_WSUM..: 12 warp sums of the prologue scan.
+// M_HEAD, M_TAIL: (request, head, first row, q_len, first CTA, CTA count) of each.
+// M_TMEM: TMEM base address of the tcgen05 kernel.  M_ZERO: a 16-byte line of zeros.
+// M_QHDR: (request, KV head, q_len, first row, context) of the request whose query sits
+// in query slot k, at M_QHDR + 8 k; written by the producer with the request's first tile.
+// M_F0, M_F0 + 1: the merge generation of the head / tail sequence read before arriving.
+// M_VCTA: the CTA's place in the schedule (its partial slots and share of a merge).
+enum : int {
+  M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24, M_TMEM = 30,
+  M_ZERO = 32, M_QHDR = 40, M_F0 = 56, M_VCTA = 58
+};
+constexpr int kMiscBytes = 256;
+
 // ------------------------------------------------------------------ per-request geometry
 
 struct ReqInfo {
@@ -142,7 +157,30 @@ __device__ __forceinline__ ReqInfo request_info(const KParams &p, int r, uint32_
   return ri;
 }
 
-// The CTA's tile range [a, b).
+// Sequence-aligned schedule: place c (< cst[B]) is chunk j of the k CTAs of sequence
+// (r, h), whose nt tiles start at global tile gs.
+__device__ __forceinline__ void aligned_seq(const KParams &p, const int32_t *tstart, int c, int &r,
+                                            int &h, int &j, int &k, int &nt, int &gs) {
+  const int B = p.num_seqs;
+  const int32_t *cst = tstart + B + 2;
+  int lo = 0, hi = B - 1;  // first r with cst[r + 1] > c
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (cst[mid + 1] > c)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  r = lo;
+  k = (cst[r + 1] - cst[r]) / p.Hkv;
+  const int loc = c - cst[r];
+  h = loc / k;
+  j = loc - h * k;
+  nt = tstart[r + 1] - tstart[r];
+  gs = tstart[r] * p.Hkv + h * nt;
+}
+
+// The tile range [a, b) of schedule place c.
 __device__ __forceinline__ void cta_range(const KParams &p, const int32_t *tstart, int c, int &a,
                                        int &b) {
   const int B = p.num_seqs, T = tstart[B] * p.Hkv;
@@ -151,17 +189,8 @@ __device__ __forceinline__ void cta_range(const KParams &p, const int32_t *tstar
     if (cst[B + 1]) {  // sequence-aligned: chunk j of the k CTAs of sequence (r, h)
       a = b = T;
       if (c >= cst[B]) return;
-      int lo = 0, hi = B - 1;  // first r with cst[r + 1] > c
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (cst[mid + 1] > c)
-          hi = mid;
-        else
-          lo = mid + 1;
-      }
-      const int r = lo, k = (cst[r + 1] - cst[r]) / p.Hkv, loc = c - cst[r];
-      const int h = loc / k, j = loc - h * k, nt = tstart[r + 1] - tstart[r];
-      const int gs = tstart[r] * p.Hkv + h * nt;
+      int r, h, j, k, nt, gs;
+      aligned_seq(p, tstart, c, r, h, j, k, nt, gs);
       const int s_last = cst[B + 1] >> 1;
       if (s_last > 0 && h == p.Hkv - 1 && cst[r + 1] == cst[B]) {
         // the grid's last sequence: its last CTA takes s_last tiles, the others share the rest
@@ -262,7 +291,8 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
     for (int o = 16; o >= 1; o >>= 1) wt += __shfl_xor_sync(full, wt, o);
     const uint32_t G = (uint32_t)(p.grid / p.Hkv);
     bool aligned = !p.sched_partition && tstart[B] > 0 && ne <= G;
-    uint32_t lo = 1;
+    uint32_t lo = 1, kmn = 0xffffffffu, kmx = 0;  // fewest and most CTAs of a request
+    bool spread = false;                           // CTAs interleaved over the sequences
     if (aligned) {
       // lower bound: the average work per CTA; upper bounds that are feasible: the largest
       // request (one CTA each), and W / (G - E) (sum ceil(w / X) < W / X + E <= G).
@@ -310,6 +340,10 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
           cst[r] = k;
         }
         tot += (uint32_t)k;
+        if (k > 0) {
+          kmn = min(kmn, (uint32_t)k);
+          kmx = max(kmx, (uint32_t)k);
+        }
         const unsigned used = __ballot_sync(full, k > 0);
         if (used) {
           const int top = 31 - __clz(used);
@@ -318,13 +352,18 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
         }
       }
       tot = __reduce_add_sync(full, tot);
+      kmn = __reduce_min_sync(full, kmn);
+      kmx = __reduce_max_sync(full, kmx);
       __syncwarp();
       // With no CTA left over, the last CTA of the grid starts last (after the previous
       // launch's final merge and its own prologue, some 6 tile-times at one query token):
       // it takes fewer tiles.  (CTAs left over sit at the end of the grid and take those
       // late SMs themselves.)
+      // With every CTA in use and the same K >= 2 CTAs for every sequence, the CTAs are
+      // interleaved instead (below), and those placed last start with fewer tiles.
+      spread = tot == G && kmn == kmx && kmx >= 2;
       int s_last = 0;
-      if (tot == G && r_last >= 0) {
+      if (!spread && tot == G && r_last >= 0) {
         const int nt = tstart[r_last + 1] - tstart[r_last], k = cst[r_last];
         const int q = max(q_last, 1), pt = max(1, (6 + q / 2) / q);
         if (k >= 2) s_last = max(1, nt / k - pt);
@@ -351,10 +390,35 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
     }
     __syncwarp();
     if (lane == 0) {  // this CTA's range, for every thread (wsum is free by now)
-      int a, b;
-      cta_range(p, tstart, blockIdx.x, a, b);
+      int a, b, v = blockIdx.x;
+      if (spread) {
+        // The CTAs of the grid start in index order as SMs free up, and the last K of
+        // them take the SMs of the previous launch's last sequence to finish.  So CTA c
+        // plays chunk j = c / S of sequence c mod S (S sequences of K chunks), which spreads
+        // those late CTAs over every sequence, and a sequence's chunks of CTAs c >= U - K
+        // (its last m ones) each take d tiles fewer than the others: some 2 tile-times at
+        // one query token, which is how late they then start.
+        const int U = cst[B], K = (int)kmx, S = U / K;
+        const int sq = (int)blockIdx.x % S, j = (int)blockIdx.x / S;
+        v = sq * K + j;
+        int r, h, jj, k, nt, gs;
+        aligned_seq(p, tstart, v, r, h, jj, k, nt, gs);
+        const int first_late = max(0, (U - K - sq + S - 1) / S);  // first j with c >= U - K
+        const int m = K - min(K, first_late);
+        const int q = max((int)qm, 1);
+        const int d = min(max(1, (2 + q / 2) / q), nt / (2 * K));
+        auto start = [&](int x) {  // first tile of chunk x
+          const int64_t num = (int64_t)x * (nt + m * d) - (int64_t)d * K * max(0, x - (K - m));
+          return (int)(num / K);
+        };
+        a = gs + start(j);
+        b = gs + start(j + 1);
+      } else {
+        cta_range(p, tstart, v, a, b);
+      }
       wsum[0] = a;
       wsum[1] = b;
+      wsum[M_VCTA - M_WSUM] = v;
     }
   }
   __syncthreads();
@@ -443,19 +507,6 @@ struct Smem {
   __device__ int32_t *misc() const { return misc_p; }
 };
 
-// misc[] words
-// M_LAST, M_LAST + 1: merge duty for the head / tail sequence; M_WCNT: writer warps that
-// have stored their part of the head partial; M_WSUM..: 12 warp sums of the prologue scan.
-// M_HEAD, M_TAIL: (request, head, first row, q_len, first CTA, CTA count) of each.
-// M_TMEM: TMEM base address of the tcgen05 kernel.  M_ZERO: a 16-byte line of zeros.
-// M_QHDR: (request, KV head, q_len, first row, context) of the request whose query sits
-// in query slot k, at M_QHDR + 8 k; written by the producer with the request's first tile.
-// M_F0, M_F0 + 1: the merge generation of the head / tail sequence read before arriving.
-enum : int {
-  M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24, M_TMEM = 30,
-  M_ZERO = 32, M_QHDR = 40, M_F0 = 56
-};
-constexpr int kMiscBytes = 256;
 
 // Waits for stage s to hold CTA tile gt (fill parity `parity`).  A consumer that skipped
 // the stage's previous tile may find that fill not yet landed, which the parity alone

@@ -545,7 +545,7 @@ __device__ void run_softmax(const KParams &p, const Smem &sm, const UBars &ub, i
       const int nt = tstart[r + 1] - tstart[r];
       const int gs = tstart[r] * p.Hkv + h * nt;
       seq_ctas(p, tstart, r, h, gs, gs + nt, c_first, nc);
-      slot = slot_of(blockIdx.x, c_first);
+      slot = slot_of(sm.misc()[M_VCTA], c_first);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
