@@ -102,7 +102,7 @@ def csrc_sha256():
 
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
 # The indexer's two launches of one call (score + select), from the same kind of capture.
-MEASURED_TRAFFIC_INDEXER = {"bytes": 556972800, "src_sha256": "be874bcee95dbc254a2928240b2d519670ef674cbc7b3e9b0900f6b6b28592f0"}
+MEASURED_TRAFFIC_INDEXER = {"bytes": 557077760, "src_sha256": "615f9b36481d96b8d3092f217f04fd82f3c0a69bb4a7064b794e55eea6f4e44d"}
 MEASURED_TRAFFIC_KV_WRITE = {"bytes": 171386368, "src_sha256": "c0729fd8a04a448779a9dd040359180d545aa1e7f4dfb1cf5afe0cdbaae6cb6f"}
 
 

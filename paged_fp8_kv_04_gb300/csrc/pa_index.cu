@@ -10,6 +10,7 @@
 // first topk.  HBM-bound on the index cache: 128 B per position per request.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -24,12 +25,20 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kWarps = 8;           // warps per CTA of the score kernel
-constexpr int kPagesPerWarp = 4;    // pages each warp of the score kernel scores
+constexpr int kMaxPagesPerWarp = 32;  // pages one warp of the score kernel scores (one per lane)
+// A step of the score kernel: kStepTiles n-tiles (8 positions each) of one page, their
+// codes and scales, staged through a ring of kSteps slots per warp with cp.async.
+constexpr int kStepTiles = 4;
+constexpr int kSteps = 3;
+constexpr int kStepRows = 8 * kStepTiles;
+constexpr int kStepBytes = (kStepRows * kD + kStepRows * 4 + 127) / 128 * 128;
+static_assert(kStepRows <= 32, "a step's scales are one per lane");
+constexpr int kRingBytes = kWarps * kSteps * kStepBytes;
 constexpr int kQRow = 144;          // halves per staged query row (72 words)
 constexpr int kMaxRowHeads = 16;    // q_len * index_heads of one request
 constexpr int kMaxStride = 16384;   // pages per row the selection sorts
 constexpr int kMaxTopk = 1024;
-constexpr int kMaxDevices = 64;     // devices whose selection-kernel opt-in is tracked
+constexpr int kMaxDevices = 64;     // devices whose kernel opt-ins and SM count are tracked
 
 struct IdxParams {
   const uint16_t *q;
@@ -41,16 +50,10 @@ struct IdxParams {
   uint32_t *status;
   int64_t num_pages;
   int32_t B, R, H, ps, ps_shift, topk, stride, maxq;
+  int32_t ppw;   // pages per warp of the score kernel: CTA x of a request scores pages
+                 // [x kWarps ppw, (x + 1) kWarps ppw)
   float cscale;  // sm_scale * log2(e)
 };
-
-__device__ __forceinline__ uint4 load_nc16(const void *ptr) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(ptr));
-  return r;
-}
 
 // Request blockIdx.y, pages blockIdx.x * kWarps + warp.  The request's q_len * heads
 // query rows (at most 16, padded with zeros) are the M = 16 rows of mma.sync m16n8k16 in
@@ -58,8 +61,12 @@ __device__ __forceinline__ uint4 load_nc16(const void *ptr) {
 // columns, 8 per n-tile; its e4m3 codes widen exactly to f16.  The reduction index is
 // permuted: in k-step kk, lane (g, t) supplies real dimensions 32 t + 4 kk + 0..3 for both
 // operands, so each lane reads 32 contiguous bytes of a token row and the four lanes of a
-// quad cover the whole 128-byte row.
+// quad cover the whole 128-byte row.  Each warp streams its pages through its own ring of
+// kSteps shared-memory slots with cp.async, two steps ahead of the one it computes (the
+// 16-byte chunks of a row are XOR-swizzled by the row, so the quads' reads meet no bank
+// conflict), which keeps twice the bytes of a register double buffer in flight.
 __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxParams p) {
+  extern __shared__ __align__(128) uint8_t ring[];
   // f16 query rows in k-step order: row, k-step kk, lane column t, then the 4 dimensions
   // 32 t + 4 kk + 0..3; rows 72 words apart so that a fragment load has no bank conflict
   __shared__ __align__(16) uint16_t qh[16 * kQRow];
@@ -74,7 +81,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
   }
   if (ql == 0) return;
   const int npg = min((L + p.ps - 1) >> p.ps_shift, p.stride);
-  if ((int)blockIdx.x * kWarps * kPagesPerWarp >= npg) return;  // the same for the whole CTA
+  if ((int)blockIdx.x * kWarps * p.ppw >= npg) return;  // the same for the whole CTA
   const int nrh = ql * p.H;
   bool qbad = false;
   for (int i = threadIdx.x; i < 16 * kD; i += kWarps * 32) {
@@ -87,10 +94,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
   if (qbad && p.status != nullptr) atomicOr(p.status, PA_DEV_Q_RANGE);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  // this warp's pages: b_i = blockIdx.x * kWarps * kPagesPerWarp + warp + kWarps * i
-  const int bfirst = blockIdx.x * kWarps * kPagesPerWarp + warp;
+  // this warp's pages: b_i = blockIdx.x * kWarps * ppw + warp + kWarps * i
+  const int bfirst = blockIdx.x * kWarps * p.ppw + warp;
   int npw = 0;
-  while (npw < kPagesPerWarp && bfirst + kWarps * npw < npg) ++npw;
+  while (npw < p.ppw && bfirst + kWarps * npw < npg) ++npw;
   if (npw == 0) return;
   int my_phys = 0;  // lane i holds page i's physical page
   if (lane < npw) my_phys = p.bt[(int64_t)r * p.stride + bfirst + kWarps * lane];
@@ -113,31 +120,26 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
   const int rowA = g, rowB = g + 8;
   const int limA = rowA < nrh ? L - ql + rowA / p.H + 1 : INT_MIN;
   const int limB = rowB < nrh ? L - ql + rowB / p.H + 1 : INT_MIN;
-  const int ntiles = p.ps >> 3, ngr = (ntiles + 3) >> 2, total = npw * ngr;
+  const int ntiles = p.ps >> 3, ngr = (ntiles + kStepTiles - 1) / kStepTiles, total = npw * ngr;
 
-  struct Buf {
-    uint4 raw[4][2];
-    float ks[4][2];
-  };
-  // loads of step `it`: page it / ngr, n-tiles 4 (it % ngr) .. + 3
-  auto load = [&](int it, Buf &bf) {
-    const int i = it / ngr, j0 = 4 * (it - i * ngr);
+  // step it: page it / ngr of the warp, n-tiles kStepTiles (it % ngr) onwards, into ring slot
+  // `slot`
+  const uint32_t wring = pa::smem_u32(ring) + warp * kSteps * kStepBytes;
+  auto issue = [&](int it, int slot) {
+    const int i = it / ngr, j0 = kStepTiles * (it - i * ngr);
     int ph = __shfl_sync(0xffffffffu, my_phys, i);
     const bool bad = __shfl_sync(0xffffffffu, my_bad ? 1 : 0, i) != 0;
     if (bad) ph = 0;  // read a valid page; the page's scores are written as -inf
-    const uint8_t *kp = p.k + (int64_t)ph * p.ps * kD + 32 * t;
+    const int rows = min(kStepRows, p.ps - 8 * j0);
+    const uint8_t *kp = p.k + ((int64_t)ph * p.ps + 8 * j0) * kD;
+    const uint32_t sb = wring + slot * kStepBytes;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = j0 + u;
-      if (j < ntiles) {
-        const uint8_t *row = kp + (int64_t)(8 * j + g) * kD;
-        bf.raw[u][0] = load_nc16(row);
-        bf.raw[u][1] = load_nc16(row + 16);
-        const int tk = 8 * j + 2 * t;
-        bf.ks[u][0] = p.ks != nullptr ? __ldg(p.ks + (int64_t)ph * p.ps + tk) : 1.f;
-        bf.ks[u][1] = p.ks != nullptr ? __ldg(p.ks + (int64_t)ph * p.ps + tk + 1) : 1.f;
-      }
+    for (int k = 0; k < kStepRows / 4; ++k) {
+      const int q = lane + 32 * k, x = q >> 3, c = q & 7;  // row x, 16-byte chunk c
+      if (x < rows) pa::cp_async16(sb + x * kD + ((c ^ (x & 7)) << 4), kp + x * kD + 16 * c);
     }
+    if (p.ks != nullptr && lane < rows)
+      pa::cp_async4(sb + kStepRows * kD + 4 * lane, p.ks + (int64_t)ph * p.ps + 8 * j0 + lane);
   };
   float mA = -INFINITY, zA = 0.f, mB = -INFINITY, zB = 0.f;
   auto fold = [&](float v, int pos, int lim, float &m, float &z) {
@@ -149,15 +151,18 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
       z += exp2f(v - m);
     }
   };
-  auto compute = [&](int it, const Buf &bf) {
-    const int i = it / ngr, j0 = 4 * (it - i * ngr);
+  auto compute = [&](int it, int slot) {
+    const int i = it / ngr, j0 = kStepTiles * (it - i * ngr);
     const int pos0 = (bfirst + kWarps * i) * p.ps;
+    const uint32_t sb = wring + slot * kStepBytes;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kStepTiles; ++u) {
       const int j = j0 + u;
       if (j >= ntiles) break;
-      const uint32_t w[8] = {bf.raw[u][0].x, bf.raw[u][0].y, bf.raw[u][0].z, bf.raw[u][0].w,
-                             bf.raw[u][1].x, bf.raw[u][1].y, bf.raw[u][1].z, bf.raw[u][1].w};
+      const uint32_t rb = sb + (8 * u + g) * kD;
+      const uint4 x0 = pa::lds128(rb + (((2 * t) ^ g) << 4));
+      const uint4 x1 = pa::lds128(rb + (((2 * t + 1) ^ g) << 4));
+      const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -166,7 +171,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
         pa::mma_f16(acc, af[kk], b0, b1);
       }
       const int tk = 8 * j + 2 * t;
-      const float s0 = p.cscale * bf.ks[u][0], s1 = p.cscale * bf.ks[u][1];
+      float s0 = p.cscale, s1 = p.cscale;
+      if (p.ks != nullptr) {
+        const float2 kv = pa::lds64f(sb + kStepRows * kD + 4 * (8 * u + 2 * t));
+        s0 *= kv.x;
+        s1 *= kv.y;
+      }
       fold(acc[0] * s0, pos0 + tk, limA, mA, zA);
       fold(acc[1] * s1, pos0 + tk + 1, limA, mA, zA);
       fold(acc[2] * s0, pos0 + tk, limB, mB, zB);
@@ -209,12 +219,19 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
     mA = mB = -INFINITY;
     zA = zB = 0.f;
   };
-  // (double-buffering the loads measured slower: the registers cost a CTA per SM)
+  for (int it = 0; it < kSteps - 1; ++it) {
+    if (it < total) issue(it, it);
+    pa::cp_async_commit();
+  }
   for (int it = 0; it < total; ++it) {
-    Buf bf;
-    load(it, bf);
-    compute(it, bf);
+    const int nx = it + kSteps - 1;  // refills the slot of step it - 1, read by now
+    if (nx < total) issue(nx, nx % kSteps);
+    pa::cp_async_commit();
+    pa::cp_async_wait<kSteps - 1>();  // this lane's copies of step it have landed
+    __syncwarp();                     // and so have the other lanes'
+    compute(it, it % kSteps);
     if ((it + 1) % ngr == 0) finish(it / ngr);
+    __syncwarp();  // every lane has read the slot before a later step refills it
   }
 }
 
@@ -291,6 +308,8 @@ int log2_page(int ps) {
   }
 }
 
+int g_sms[kMaxDevices];  // SM count of each device, read with its opt-ins
+
 }  // namespace
 
 extern "C" pa_status_t pa_index_topk(const pa_index_args_t *a, void *stream) {
@@ -339,27 +358,36 @@ extern "C" pa_status_t pa_index_topk(const pa_index_args_t *a, void *stream) {
   p.cscale = a->sm_scale * 1.4426950408889634f;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
   int n = 1;
   while (n < a->block_table_stride) n <<= 1;
   const size_t smem = (size_t)n * sizeof(unsigned long long);
-  if (smem > 48 * 1024) {
-    // the selection kernel's opt-in shared-memory limit, set once per device (the
-    // attribute belongs to the device's context)
+  {
+    // the kernels' opt-in shared-memory limits, set once per device (the attributes
+    // belong to the device's context)
     static std::once_flag once[kMaxDevices];
     static cudaError_t opt_err[kMaxDevices];
-    int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
     std::call_once(once[dev], [dev]() {
       opt_err[dev] = cudaFuncSetAttribute(index_select_kernel,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)(kMaxStride * sizeof(unsigned long long)));
+      if (opt_err[dev] == cudaSuccess)
+        opt_err[dev] = cudaFuncSetAttribute(index_score_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (opt_err[dev] == cudaSuccess)
+        opt_err[dev] = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     });
     if (opt_err[dev] != cudaSuccess) return PA_ERR_CUDA;
   }
-  const int gx = (a->block_table_stride + kWarps * kPagesPerWarp - 1) / (kWarps * kPagesPerWarp);
+  // One wave of score CTAs (two per SM): gx CTAs per request, each warp scoring ppw pages.
+  const int stride = a->block_table_stride;
+  int gx = std::max(1, 2 * g_sms[dev] / p.B);
+  p.ppw = std::min(kMaxPagesPerWarp, (stride + kWarps * gx - 1) / (kWarps * gx));
+  gx = (stride + kWarps * p.ppw - 1) / (kWarps * p.ppw);
   (void)cudaGetLastError();  // drop an earlier, unrelated launch error
-  index_score_kernel<<<dim3(gx, p.B), kWarps * 32, 0, s>>>(p);
+  index_score_kernel<<<dim3(gx, p.B), kWarps * 32, kRingBytes, s>>>(p);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   const int threads = n >= 2048 ? 1024 : (n >= 64 ? n / 2 : 32);
   index_select_kernel<<<a->num_rows, threads, smem, s>>>(p, n);
