@@ -125,38 +125,46 @@ pa_status_t geometry(const pa_plan_desc_t *d, Geometry *g) {
   g->stage_bytes = d->kv_dtype == PA_KV_FP8_E4M3 ? (2 * pa::kTile * pa::kD + 1024)
                                                  : (4 * pa::kTile * pa::kD);
   g->qslot_bytes = d->q_len * pa::kQRowBytes;
-  // the exchange buffer (mid-stream ends; the CTA's last merge runs in stage memory): 4
+  // The exchange buffer (mid-stream ends; the CTA's last merge runs in stage memory) has 4
   // slots, or 2 for plans of at most two query tokens on the mma.sync kernel (a round moves
-  // whole slices, q_len m-tiles each), which leaves room for one more stage
-  g->xslots = (d->q_len <= 2 && !use_umma(*d)) ? kSmallXSlots : 4;
-  const size_t merge_bytes = (size_t)g->xslots * (8192 + 512);
-  for (int ns = 6; ns >= 2; --ns) {
-    size_t off = (size_t)ns * g->stage_bytes;
-    const size_t off_q = off;
-    off += 2 * (size_t)g->qslot_bytes;
-    const size_t off_merge = off;
-    off += merge_bytes;
-    const size_t off_tstart = off;
-    off += round_up((size_t)(2 * d->max_batch + 4) * 4, 16);  // tstart, then the CTA prefix
-    const size_t off_meta = off;
-    off += (size_t)ns * sizeof(pa::StageMeta);
-    const size_t off_bar = off;
-    off += round_up((size_t)(2 * ns + 3 + pa::kUmmaBars) * 8, 16);
-    const size_t off_misc = off;
-    off += pa::kMiscBytes;
-    const size_t total = off + 1024;  // slack for the 1024-byte alignment of the base
-    if (total <= (size_t)smem_max) {
-      g->nstage = ns;
-      g->off_q = (int)off_q;
-      g->off_merge = (int)off_merge;
-      g->off_tstart = (int)off_tstart;
-      g->off_meta = (int)off_meta;
-      g->off_bar = (int)off_bar;
-      g->off_misc = (int)off_misc;
-      g->smem = total;
-      break;
+  // whole slices, q_len m-tiles each) where that leaves room for one more stage: two slots
+  // take more rounds per mid-stream end.
+  auto fit = [&](int xslots, bool commit) {
+    const size_t merge_bytes = (size_t)xslots * (8192 + 512);
+    for (int ns = 6; ns >= 2; --ns) {
+      size_t off = (size_t)ns * g->stage_bytes;
+      const size_t off_q = off;
+      off += 2 * (size_t)g->qslot_bytes;
+      const size_t off_merge = off;
+      off += merge_bytes;
+      const size_t off_tstart = off;
+      off += round_up((size_t)(2 * d->max_batch + 4) * 4, 16);  // tstart, then the CTA prefix
+      const size_t off_meta = off;
+      off += (size_t)ns * sizeof(pa::StageMeta);
+      const size_t off_bar = off;
+      off += round_up((size_t)(2 * ns + 3 + pa::kUmmaBars) * 8, 16);
+      const size_t off_misc = off;
+      off += pa::kMiscBytes;
+      const size_t total = off + 1024;  // slack for the 1024-byte alignment of the base
+      if (total <= (size_t)smem_max) {
+        if (commit) {
+          g->xslots = xslots;
+          g->nstage = ns;
+          g->off_q = (int)off_q;
+          g->off_merge = (int)off_merge;
+          g->off_tstart = (int)off_tstart;
+          g->off_meta = (int)off_meta;
+          g->off_bar = (int)off_bar;
+          g->off_misc = (int)off_misc;
+          g->smem = total;
+        }
+        return ns;
+      }
     }
-  }
+    return 0;
+  };
+  const bool small = d->q_len <= 2 && !use_umma(*d);
+  fit(small && fit(kSmallXSlots, false) > fit(4, false) ? kSmallXSlots : 4, true);
   if (g->nstage == 0) return PA_ERR_UNSUPPORTED;
 
   size_t off = 0;

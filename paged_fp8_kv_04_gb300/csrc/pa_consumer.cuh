@@ -104,15 +104,17 @@ __device__ __forceinline__ void reset_state(Frag &f) {
 }
 
 // Per-token V scales fold into P per row: P'[j] = p[j] * v_scale[j] * 2^pe, with one power
-// of two per row (and lane quad).  When it is set, the chunk's largest p * v_scale * 2^pe
-// lands in [2^6, 2^7); it is kept while that stays within [2^-6, 2^12).  So P' never
-// overflows the f16 operand, and the largest terms of every chunk keep f16's 11 bits,
-// however far apart the tokens' magnitudes (per-token scales of 2^-20 .. 2^20 in one
-// sequence included): the reference is the largest product, not the largest scale, so a
-// token with p = 1 and a small scale is not flushed by a neighbour with a large scale and
-// p ~ 0.  The row's o is accumulated in the same units.  The power of two rides in the
-// exponent of p (online_row_pe), so the common case costs one multiply per term, as a
-// fixed fold would; pe stays within [-60, 60], which covers V scales of 2^-60 .. 2^64.
+// of two per row (and lane quad), kept while the chunk's largest p * v_scale * 2^pe stays
+// within [2^-6, 2^12).  So P' never overflows the f16 operand, and the largest terms of
+// every chunk keep f16's 11 bits, however far apart the tokens' magnitudes (per-token
+// scales of 2^-20 .. 2^20 in one sequence included): the reference is the largest product,
+// not the largest scale, so a token with p = 1 and a small scale is not flushed by a
+// neighbour with a large scale and p ~ 0.  The row's o is accumulated in the same units,
+// and the power of two rides in the exponent of p.  pe is chosen from the chunk's V-scale
+// exponent range and the row's largest p' (online_row_fit), known before the exponentials,
+// without a branch between the softmax and PV; only a chunk whose scales spread wider than
+// 2^15 (or that holds masked tokens) takes an exact test of its P' (refold_row).  pe stays
+// within [-60, 60], which covers V scales of 2^-60 .. 2^64.
 constexpr int kPeMin = -60, kPeMax = 60;
 constexpr int kScalarPe = 8;  // the fixed power of two of P in scalar-scale mode
 
@@ -140,29 +142,77 @@ __device__ __forceinline__ float online_row_pe(float (&s)[N], float &m, float &l
   return alpha;
 }
 
-// The largest of this lane's P' of row g (half 0) and row g + 8 (half 1) in the packed f16
-// fragments, as an f16x2 word, reduced over the lane quad (which holds the rows' columns).
-template <int NKS>
-__device__ __forceinline__ uint32_t packed_row_max(const uint32_t (&pa)[NKS][4]) {
-  uint32_t r0 = hmax2(pa[0][0], pa[0][2]), r1 = hmax2(pa[0][1], pa[0][3]);
-#pragma unroll
-  for (int ks = 1; ks < NKS; ++ks) {
-    r0 = hmax2(r0, hmax2(pa[ks][0], pa[ks][2]));
-    r1 = hmax2(r1, hmax2(pa[ks][1], pa[ks][3]));
-  }
-  // (lo, hi) of each row -> one word: row g's maximum in the low half, row g + 8's in the high
-  uint32_t w = hmax2(prmt(r0, r1, 0x5410), prmt(r0, r1, 0x7632));
-  w = hmax2(w, __shfl_xor_sync(~0u, w, 1));
-  w = hmax2(w, __shfl_xor_sync(~0u, w, 2));
-  return w;
+// floor(log2 x) of a positive normal float, from its exponent field; -1000 for 0.
+__device__ __forceinline__ int ilog2f(float x) {
+  return x > 0.f ? (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127 : -1000;
 }
 
-// An f16 row maximum inside [2^-6, 2^12): 0x2400 <= bits < 0x6C00 (sign clear; f16's
-// exponent field holds e + 15).
-__device__ __forceinline__ bool in_window(uint32_t h) { return h >= 0x2400u && h < 0x6C00u; }
+// floor(log2) of the smallest and the largest of the chunk's V weights.  Every lane quad
+// holds all of the chunk's tokens, so a reduction over the whole warp (one redux per
+// bound) gives the chunk's range, the same in every lane.
+template <int N>
+__device__ __forceinline__ void weight_exponents(const float (&w)[N], int &el, int &eh) {
+  float a[N / 2], b[N / 2];
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    a[k] = fminf(w[2 * k], w[2 * k + 1]);
+    b[k] = fmaxf(w[2 * k], w[2 * k + 1]);
+  }
+#pragma unroll
+  for (int n = N / 4; n >= 1; n >>= 1) {  // a tree: log2 N dependent steps
+#pragma unroll
+    for (int k = 0; k < n; ++k) {
+      a[k] = fminf(a[k], a[k + n]);
+      b[k] = fmaxf(b[k], b[k + n]);
+    }
+  }
+  el = __reduce_min_sync(~0u, ilog2f(a[0]));
+  eh = __reduce_max_sync(~0u, ilog2f(b[0]));
+}
 
-// The row's P' (in s, fp32) left its window: a new pe from the fp32 maximum (0 keeps it).
-// Returns the factor P' and the row's o are rescaled by.
+// online_row_pe for a chunk whose V weights lie in [2^el, 2^(eh + 1)) with eh - el <= 15:
+// the row's largest P' then lies in [2^(top + el), 2^(top + eh + 1)), top the log2 of its
+// largest p'.  When that interval leaves the window [2^-6, 2^12), pe moves (and the
+// returned factor rescales o) so that its upper end lands in (2^(T - 1), 2^T], T = (7 +
+// eh - el) / 2, the middle of the room the window leaves; its lower end then stays above
+// 2^-6.  No test of P' itself, and no branch between the softmax and PV.
+template <int N>
+__device__ __forceinline__ float online_row_fit(float (&s)[N], float &m, float &l, int &pe,
+                                                int eh, int el) {
+  float mx = s[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) mx = fmaxf(mx, s[k]);
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
+  float alpha = 1.f;
+  if (mx > m) {
+    alpha = fast_exp2(m - mx);
+    m = mx;
+    l *= alpha;
+  }
+  if (mx != -INFINITY) {
+    const float top = mx - m + (float)pe;
+    const float hb = top + (float)(eh + 1), lb = top + (float)el;
+    if (hb > 12.f || lb < -6.f) {
+      const int T = (7 + eh - el) >> 1;
+      const int ne = min(max(pe + T - (int)ceilf(hb), kPeMin), kPeMax);
+      alpha *= __uint_as_float((uint32_t)(ne - pe + 127) << 23);
+      pe = ne;
+    }
+  }
+  const float ref = ((m == -INFINITY) ? 0.f : m) - (float)pe;
+#pragma unroll
+  for (int k = 0; k < N; ++k) s[k] = fast_exp2(s[k] - ref);
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < N; k += 4) sum += (s[k] + s[k + 1]) + (s[k + 2] + s[k + 3]);
+  l += sum * __uint_as_float((uint32_t)(127 - pe) << 23);
+  return alpha;
+}
+
+// The row's P' (in s, fp32) checked against the window [2^-6, 2^12): outside it, a new pe
+// from the fp32 maximum that puts it in [2^6, 2^7) (0 keeps it).  Returns the factor P' and
+// the row's o are rescaled by.
 template <int N>
 __device__ __forceinline__ float refold_row(float (&s)[N], int &pe) {
   float wmax = 0.f;
@@ -390,30 +440,39 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
     if (SM == PA_SCALE_PER_TOKEN) mask_weights<NC>(vw, pos0, cut);
   }
   uint32_t pa[NKS][4];
+  float a0, a1;
   if (SM == PA_SCALE_PER_TOKEN) {
-    float a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], f.pe[0]);
-    float a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], f.pe[1]);
+    int el, eh;
+    weight_exponents<NC>(vw, el, eh);  // ready long before the softmax needs it
+    if (eh - el <= 15) {  // the same for the whole warp
+      a0 = online_row_fit<NC>(s0, f.m[0], f.l[0], f.pe[0], eh, el);
+      a1 = online_row_fit<NC>(s1, f.m[1], f.l[1], f.pe[1], eh, el);
 #pragma unroll
-    for (int k = 0; k < NC; ++k) {
-      s0[k] *= vw[k];
-      s1[k] *= vw[k];
-    }
-    pack_p<NC>(s0, s1, false, pa);
-    const uint32_t wm = packed_row_max<NKS>(pa);
-    if (__any_sync(~0u, !(in_window(wm & 0xFFFFu) && in_window(wm >> 16)))) {  // rare
+      for (int k = 0; k < NC; ++k) {
+        s0[k] *= vw[k];
+        s1[k] *= vw[k];
+      }
+    } else {
+      // scales spread wider (or masked tokens, whose weight is 0): each row's window is
+      // settled on its fp32 P'
+      a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], f.pe[0]);
+      a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], f.pe[1]);
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        s0[k] *= vw[k];
+        s1[k] *= vw[k];
+      }
       a0 *= refold_row<NC>(s0, f.pe[0]);
       a1 *= refold_row<NC>(s1, f.pe[1]);
-      pack_p<NC>(s0, s1, false, pa);
     }
-    rescale_rows(f.o, a0, a1);
   } else {
     // one scale for the whole cache: P' = p * 2^8 (p <= 1) keeps p down to 2^-22 out of
     // f16's subnormals; the host folds 2^-8 into the V scale applied at the end
-    const float a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], kScalarPe);
-    const float a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], kScalarPe);
-    rescale_rows(f.o, a0, a1);
-    pack_p<NC>(s0, s1, false, pa);
+    a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], kScalarPe);
+    a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], kScalarPe);
   }
+  pack_p<NC>(s0, s1, false, pa);
+  rescale_rows(f.o, a0, a1);
 #pragma unroll
   for (int ks = 0; ks < NKS; ++ks) {
     const int rv = tb + 16 * ks + 2 * t;

@@ -318,7 +318,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     if (!mine_k) continue;
     const int32_t *rec = sm.misc() + (k == 0 ? M_HEAD : M_TAIL);
     const int hh = rec[1];
-    if (kShareMerge && p.coresident) {
+    if (kShareMerge && p.coresident && rec[5] * rec[3] >= kShareMin) {
       // every CTA of the sequence takes a share of its merge once all have arrived
       if (!sm.misc()[M_LAST + k]) {
         if (ctid == 0) {
@@ -330,7 +330,8 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       }
       merge_share<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], sm.misc()[M_VCTA] - rec[4], ctid);
     } else if (sm.misc()[M_LAST + k]) {
-      // CTAs of one sequence may run in different waves: the last to arrive merges alone
+      // a small merge, or CTAs of one sequence in different waves: the last to arrive merges
+      // alone (the others exit, and the next launch's CTAs take their SMs meanwhile)
       __threadfence();
       merge_partials<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], ctid);
     }

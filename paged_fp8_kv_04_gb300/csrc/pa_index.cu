@@ -40,6 +40,21 @@ constexpr int kMaxStride = 16384;   // pages per row the selection sorts
 constexpr int kMaxTopk = 1024;
 constexpr int kMaxDevices = 64;     // devices whose kernel opt-ins and SM count are tracked
 
+// Asynchronous global -> shared copies of 16 bytes (through L2 only) and of 4 bytes; each
+// thread tracks its own copies in commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's commit groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 struct IdxParams {
   const uint16_t *q;
   const uint8_t *k;
@@ -136,10 +151,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
 #pragma unroll
     for (int k = 0; k < kStepRows / 4; ++k) {
       const int q = lane + 32 * k, x = q >> 3, c = q & 7;  // row x, 16-byte chunk c
-      if (x < rows) pa::cp_async16(sb + x * kD + ((c ^ (x & 7)) << 4), kp + x * kD + 16 * c);
+      if (x < rows) cp_async16(sb + x * kD + ((c ^ (x & 7)) << 4), kp + x * kD + 16 * c);
     }
     if (p.ks != nullptr && lane < rows)
-      pa::cp_async4(sb + kStepRows * kD + 4 * lane, p.ks + (int64_t)ph * p.ps + 8 * j0 + lane);
+      cp_async4(sb + kStepRows * kD + 4 * lane, p.ks + (int64_t)ph * p.ps + 8 * j0 + lane);
   };
   float mA = -INFINITY, zA = 0.f, mB = -INFINITY, zB = 0.f;
   auto fold = [&](float v, int pos, int lim, float &m, float &z) {
@@ -221,13 +236,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
   };
   for (int it = 0; it < kSteps - 1; ++it) {
     if (it < total) issue(it, it);
-    pa::cp_async_commit();
+    cp_async_commit();
   }
   for (int it = 0; it < total; ++it) {
     const int nx = it + kSteps - 1;  // refills the slot of step it - 1, read by now
     if (nx < total) issue(nx, nx % kSteps);
-    pa::cp_async_commit();
-    pa::cp_async_wait<kSteps - 1>();  // this lane's copies of step it have landed
+    cp_async_commit();
+    cp_async_wait<kSteps - 1>();  // this lane's copies of step it have landed
     __syncwarp();                     // and so have the other lanes'
     compute(it, it % kSteps);
     if ((it + 1) % ngr == 0) finish(it / ngr);

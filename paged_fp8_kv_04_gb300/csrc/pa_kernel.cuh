@@ -48,6 +48,9 @@ constexpr int kMaxQ = 8;         // most query tokens per request (m-tiles)
 // or pair through the exchange buffer (false).  A sequence split across co-resident CTAs:
 // every one of them merges a share of it (true), or the last to arrive merges it (false).
 constexpr bool kSlotMerge = true, kShareMerge = true;
+// A shared merge needs this many partial m-tiles (CTAs x query tokens) of the sequence;
+// smaller ones are merged by the last CTA to arrive.
+constexpr int kShareMin = 8;
 constexpr int kQRowBytes = kG * kD * 2;   // one query token's 16 heads, bf16
 constexpr int kMergeBytes = 4 * 8192 + 4 * 512;  // the exchange buffer at 4 slots
 constexpr int kUmmaBars = 24;    // extra mbarriers of the tcgen05 kernel

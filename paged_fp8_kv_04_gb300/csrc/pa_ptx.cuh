@@ -92,23 +92,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   return true;
 }
 
-// ------------------------------------------------------------------- cp.async (LDGSTS)
-
-// Asynchronous global -> shared copies of 16 bytes (through L2 only) and of 4 bytes; each
-// thread tracks its own copies in commit groups.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Waits until at most N of this thread's commit groups are still in flight.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // -------------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
@@ -339,13 +322,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint
       "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(x));
-}
-
-// Lane-wise maximum of two f16x2 words.
-__device__ __forceinline__ uint32_t hmax2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

@@ -30,11 +30,18 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def run_gpu(ip, status=True):
+def run_gpu(ip, status=True, scales_4b_aligned=False):
+    """scales_4b_aligned: k_scale starts 4 bytes past a 16-byte boundary (the contract asks
+    for 4-byte alignment only)."""
     dev = lambda a, dt=None: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     q = dev(ip.q.view(np.int16))
     kc = dev(ip.k_cache)
     ks = None if ip.k_scale is None else dev(ip.k_scale)
+    if ks is not None and scales_4b_aligned:
+        buf = torch.empty(ks.numel() + 4, dtype=torch.float32, device="cuda")
+        ks = buf[1:1 + ks.numel()].view(ks.shape)
+        ks.copy_(dev(ip.k_scale))
+        assert ks.data_ptr() % 16 == 4
     bt, L, cu = dev(ip.block_table), dev(ip.context_lens), dev(ip.cu_seqlens_q)
     R, stride = ip.num_rows, ip.block_table.shape[1]
     sel = torch.full((R, ip.topk), -7, dtype=torch.int32, device="cuda")
@@ -79,8 +86,8 @@ def check_row(g, o, gS, oS, n, what):
     assert all(sc[i + 1] <= sc[i] + TOL for i in range(len(sc) - 1)), f"{what}: order rises"
 
 
-def check(ip, reqs=None, what=""):
-    gsel, gn, gS, st = run_gpu(ip)
+def check(ip, reqs=None, what="", **kw):
+    gsel, gn, gS, st = run_gpu(ip, **kw)
     assert st == 0, f"{what}: device flags {st:#x}"
     q, rows = (ip, np.arange(ip.num_rows)) if reqs is None else sub(ip, reqs)
     osel, on, oS = O.index_topk(q)
@@ -104,6 +111,20 @@ def test_index_topk(case):
     else:
         ip = synth.index_problem(44, [100, 64, 16], [1, 2, 1], page_size=16, topk=64)
     check(ip, what=case)
+
+
+@pytest.mark.parametrize("case", ["ragged_two_heads", "page128"])
+def test_index_topk_scales_4b_aligned(case):
+    """The same results when the scales are only 4-byte aligned."""
+    if case == "ragged_two_heads":
+        ip = synth.index_problem(41, [300, 1000, 37, 129], [1, 3, 2, 1], index_heads=2,
+                                 page_size=16, topk=8)
+    else:
+        ip = synth.index_problem(42, [9000, 131, 20000, 128], [1, 1, 1, 1], page_size=128, topk=16)
+    check(ip, what=case + " (4-byte aligned scales)", scales_4b_aligned=True)
+    a, an, aS, _ = run_gpu(ip)
+    b, bn, bS, _ = run_gpu(ip, scales_4b_aligned=True)
+    assert np.array_equal(an, bn) and np.array_equal(a, b) and np.array_equal(aS, bS)
 
 
 def test_index_topk_full_size_sampled():
