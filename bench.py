@@ -65,13 +65,13 @@ def parse():
 # (sha256 over the code, comments stripped, of the C header and the decode kernels'
 # translation unit); any other code gives traffic null.
 MEASURED_TRAFFIC = {
-    "long128k": {"bytes": 279804928, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
-    "long128k_scalar": {"bytes": 271451392, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
-    "dense8k": {"bytes": 69855232, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
-    "bf16ctl": {"bytes": 137147648, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
-    "ragged": {"bytes": 143990784, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
-    "sparse": {"bytes": 70664448, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
-    "prefill": {"bytes": 11231232, "csrc_sha256": "5cd22dea30a5d4fd667f4daf4d6eaccefa97abdec88d8e81e532f509908f5d6a"},
+    "long128k": {"bytes": 279792896, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
+    "long128k_scalar": {"bytes": 271406592, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
+    "dense8k": {"bytes": 70021120, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
+    "bf16ctl": {"bytes": 137195776, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
+    "ragged": {"bytes": 144063488, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
+    "sparse": {"bytes": 70827008, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
+    "prefill": {"bytes": 11290624, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
 }
 
 
@@ -102,7 +102,7 @@ def csrc_sha256():
 
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
 # The indexer's two launches of one call (score + select), from the same kind of capture.
-MEASURED_TRAFFIC_INDEXER = {"bytes": 557077760, "src_sha256": "615f9b36481d96b8d3092f217f04fd82f3c0a69bb4a7064b794e55eea6f4e44d"}
+MEASURED_TRAFFIC_INDEXER = {"bytes": 557502464, "src_sha256": "10e4ffc6dc675f80623de23a95ba07fa360db36ae91dea431676200ce5b4bf4c"}
 MEASURED_TRAFFIC_KV_WRITE = {"bytes": 171386368, "src_sha256": "c0729fd8a04a448779a9dd040359180d545aa1e7f4dfb1cf5afe0cdbaae6cb6f"}
 
 
