@@ -53,6 +53,10 @@ def parse():
                     help="FP8 plans with one query token: run the tcgen05 kernel (PA_PLAN_TCGEN05)")
     ap.add_argument("--profile", type=int, default=0,
                     help="only run --warmup + this many direct pa_decode calls (for ncu)")
+    ap.add_argument("--pools", type=int, default=0,
+                    help="with --profile: this many KV copies instead of the rotation's "
+                         "(ncu flushes L2 before each captured launch, so one copy keeps a "
+                         "capture's device memory small)")
     ap.add_argument("--only", action="store_true",
                     help="time the selected workload only (no 'workloads' key)")
     ap.add_argument("--extra-steps", type=int, default=200,
@@ -415,7 +419,7 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def _decode_setup(name, dev, tcgen05=False, partition=0):
+def _decode_setup(name, dev, tcgen05=False, partition=0, pools=0):
     """Problem, plan and rotating KV copies of a decode workload on the device."""
     import torch
     from paged_fp8_kv_04_gb300 import device as dv
@@ -430,6 +434,8 @@ def _decode_setup(name, dev, tcgen05=False, partition=0):
     touched = max(kv_bytes, 1)
     npools = max(3, int(math.ceil(3 * l2 / touched)) + 1)
     npools = min(npools, max(3, int(40e9 // max(pool_bytes, 1))))
+    if pools > 0:
+        npools = pools
     pools = [d] + [dict(d, **{k: d[k].clone() for k in ("k_cache", "v_cache", "k_scale", "v_scale")
                               if d.get(k) is not None}) for _ in range(npools - 1)]
     out = torch.empty(d["q"].shape, dtype=torch.bfloat16, device=dev)
@@ -554,7 +560,8 @@ def bench_ours(args):
         return bench_kv_write(args, dev, rank, world, local)
     if args.workload == "indexer":
         return bench_indexer(args, dev, rank, world, local)
-    w = _decode_setup(args.workload, dev, tcgen05=args.tcgen05, partition=args.partition)
+    w = _decode_setup(args.workload, dev, tcgen05=args.tcgen05, partition=args.partition,
+                      pools=args.pools if args.profile else 0)
     p, desc, plan, d, out, keep = w["p"], w["desc"], w["plan"], w["d"], w["out"], w["keep"]
     total_bytes, npools, args_list = w["total"], w["npools"], w["args_list"]
     pool_bytes, l2 = w["pool_bytes"], w["l2"]
