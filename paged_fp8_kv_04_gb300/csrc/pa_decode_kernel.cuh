@@ -110,7 +110,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
   locate(tstart, p.num_seqs, p.Hkv, a, rw, hw, tjw);
   int ntw = tstart[rw + 1] - tstart[rw];
   int seg = 0, qlen = 1, row0 = 0, L = 0, mode = 0;  // mode 0: quad, 1: paired, 2: all
-  int f0_cur = 0;  // merge generation of the current sequence (every thread holds it)
+  int f0_tail = 0;  // merge generation of the CTA's last sequence (the threads that arrive)
   for (int i = 0; i < n; ++i) {
     const int s = i % p.nstage;
     const int r = rw, h = hw, tj = tjw, nt = ntw, gt = a + i;
@@ -128,9 +128,6 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     const bool end = (i == n - 1) || (tj == nt - 1);
     const bool whole = gt - tj >= a && gt - tj + nt <= b;
     bool have = false;
-    // the merge generation of a sequence split across CTAs, read as the sequence begins here
-    // (long before this CTA counts its partial, so the load's latency is hidden)
-    if (begin && !whole) f0_cur = *reinterpret_cast<volatile int32_t *>(p.flags + r * p.Hkv + h);
     if (begin) {
       if (!wait_tile(sm, s, (i / p.nstage) & 1, gt)) {
         if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
@@ -233,6 +230,12 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     if (!end) continue;
 
     // ---- end of this CTA's part of sequence (r, h): merge the token slices -----------
+    // The merge generation of a split sequence, read by the threads that may count this
+    // CTA's partial, while the slices merge.  No arrival of this call can have bumped it:
+    // that takes every CTA of the sequence, this one included.
+    int f0 = 0;
+    if (!whole && lane == 0 && active && slice == 0)
+      f0 = *reinterpret_cast<volatile int32_t *>(p.flags + r * p.Hkv + h);
     if (SM == PA_SCALE_PER_TOKEN && active) unfold_rows(f);
     const int gs = tstart[r] * p.Hkv + h * nt;
     int c_first = blockIdx.x, nc = 1;
@@ -281,7 +284,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       rec[3] = qlen;
       rec[4] = c_first;
       rec[5] = nc;
-      sm.misc()[M_F0 + (is_head ? 0 : 1)] = f0_cur;
+      sm.misc()[M_F0 + (is_head ? 0 : 1)] = f0;
     }
     if (is_head) {
       has_head = true;
@@ -291,12 +294,13 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
           const int w = atomicAdd(&sm.misc()[M_WCNT], 1);
           if (w == mt - 1) {
             sm.misc()[M_WCNT] = 0;
-            arrive_split(p, sm, r * p.Hkv + h, nc, f0_cur, 0);
+            arrive_split(p, sm, r * p.Hkv + h, nc, f0, 0);
           }
         }
       }
     } else {
       has_tail = true;
+      f0_tail = f0;
     }
   }
 
@@ -308,7 +312,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     if (ctid == 0) {
       const int32_t *rec = sm.misc() + M_TAIL;
       __threadfence();
-      arrive_split(p, sm, rec[0] * p.Hkv + rec[1], rec[5], f0_cur, 1);
+      arrive_split(p, sm, rec[0] * p.Hkv + rec[1], rec[5], f0_tail, 1);
     }
   }
   cons_sync(p, sm, cphase);

@@ -106,7 +106,7 @@ struct KParams {
 // M_TMEM: TMEM base address of the tcgen05 kernel.  M_ZERO: a 16-byte line of zeros.
 // M_QHDR: (request, KV head, q_len, first row, context) of the request whose query sits
 // in query slot k, at M_QHDR + 8 k; written by the producer with the request's first tile.
-// M_F0, M_F0 + 1: the merge generation of the head / tail sequence read before arriving.
+// M_F0, M_F0 + 1: the merge generation of the head / tail sequence, read before arriving.
 // M_VCTA: the CTA's place in the schedule (its partial slots and share of a merge).
 enum : int {
   M_ABORT = 0, M_LAST = 1, M_WCNT = 3, M_WSUM = 4, M_HEAD = 16, M_TAIL = 24, M_TMEM = 30,
@@ -525,8 +525,8 @@ __device__ __forceinline__ bool wait_tile(const Smem &sm, int s, uint32_t parity
 }
 
 // Counts this CTA's partial of split sequence `seq` (nc CTAs): one thread, after the
-// partial's stores are fenced.  f0 is the sequence's merge generation, read when the
-// sequence began in this CTA (before any arrival of this call can have bumped it).  The
+// partial's stores are fenced.  f0 is the sequence's merge generation, read by this CTA
+// before it arrives (no arrival of this call can bump it before every CTA has).  The
 // last CTA to arrive resets the arrival counter (all have arrived) and bumps the
 // generation, which releases the CTAs that wait for it.  misc[M_LAST + k] says whether this
 // CTA was the last (k: 0 head, 1 tail).
