@@ -244,8 +244,9 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     const bool is_head = i < n - 1;
     // At the CTA's last sequence end no tile is in flight any more: every warp puts its
     // state into stage memory and all consumer threads merge the slices element by element,
-    // in one step.  Mid-stream ends pair slices through the exchange buffer.
-    const bool in_stage = kSlotMerge && !is_head && nsl > 1 && nsl * mt <= kMaxSlots &&
+    // in one step.  Mid-stream ends, and two slices (one round), pair slices through the
+    // exchange buffer.
+    const bool in_stage = kSlotMerge && !is_head && nsl > 2 && nsl * mt <= kMaxSlots &&
                           p.nstage * p.stage_bytes >= kMaxSlots * kSlotBytes;
     if (in_stage) {
       cons_sync(p, sm, cphase);  // every warp is done with its tiles

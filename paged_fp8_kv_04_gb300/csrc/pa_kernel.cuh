@@ -294,8 +294,7 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
     for (int o = 16; o >= 1; o >>= 1) wt += __shfl_xor_sync(full, wt, o);
     const uint32_t G = (uint32_t)(p.grid / p.Hkv);
     bool aligned = !p.sched_partition && tstart[B] > 0 && ne <= G;
-    uint32_t lo = 1, kmn = 0xffffffffu, kmx = 0;  // fewest and most CTAs of a request
-    bool spread = false;                           // CTAs interleaved over the sequences
+    uint32_t lo = 1;
     if (aligned) {
       // lower bound: the average work per CTA; upper bounds that are feasible: the largest
       // request (one CTA each), and W / (G - E) (sum ceil(w / X) < W / X + E <= G).
@@ -343,10 +342,6 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
           cst[r] = k;
         }
         tot += (uint32_t)k;
-        if (k > 0) {
-          kmn = min(kmn, (uint32_t)k);
-          kmx = max(kmx, (uint32_t)k);
-        }
         const unsigned used = __ballot_sync(full, k > 0);
         if (used) {
           const int top = 31 - __clz(used);
@@ -355,18 +350,13 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
         }
       }
       tot = __reduce_add_sync(full, tot);
-      kmn = __reduce_min_sync(full, kmn);
-      kmx = __reduce_max_sync(full, kmx);
       __syncwarp();
       // With no CTA left over, the last CTA of the grid starts last (after the previous
       // launch's final merge and its own prologue, some 6 tile-times at one query token):
       // it takes fewer tiles.  (CTAs left over sit at the end of the grid and take those
       // late SMs themselves.)
-      // With every CTA in use and the same K >= 2 CTAs for every sequence, the CTAs are
-      // interleaved instead (below), and those placed last start with fewer tiles.
-      spread = tot == G && kmn == kmx && kmx >= 2;
       int s_last = 0;
-      if (!spread && tot == G && r_last >= 0) {
+      if (tot == G && r_last >= 0) {
         const int nt = tstart[r_last + 1] - tstart[r_last], k = cst[r_last];
         const int q = max(q_last, 1), pt = max(1, (6 + q / 2) / q);
         if (k >= 2) s_last = max(1, nt / k - pt);
@@ -393,32 +383,9 @@ __device__ __noinline__ uint32_t scan_tiles(const KParams &p, int32_t *tstart, i
     }
     __syncwarp();
     if (lane == 0) {  // this CTA's range, for every thread (wsum is free by now)
-      int a, b, v = blockIdx.x;
-      if (spread) {
-        // The CTAs of the grid start in index order as SMs free up, and the last K of
-        // them take the SMs of the previous launch's last sequence to finish.  So CTA c
-        // plays chunk j = c / S of sequence c mod S (S sequences of K chunks), which spreads
-        // those late CTAs over every sequence, and a sequence's chunks of CTAs c >= U - K
-        // (its last m ones) each take d tiles fewer than the others: some 2 tile-times at
-        // one query token, which is how late they then start.
-        const int U = cst[B], K = (int)kmx, S = U / K;
-        const int sq = (int)blockIdx.x % S, j = (int)blockIdx.x / S;
-        v = sq * K + j;
-        int r, h, jj, k, nt, gs;
-        aligned_seq(p, tstart, v, r, h, jj, k, nt, gs);
-        const int first_late = max(0, (U - K - sq + S - 1) / S);  // first j with c >= U - K
-        const int m = K - min(K, first_late);
-        const int q = max((int)qm, 1);
-        const int d = min(max(1, (2 + q / 2) / q), nt / (2 * K));
-        auto start = [&](int x) {  // first tile of chunk x
-          const int64_t num = (int64_t)x * (nt + m * d) - (int64_t)d * K * max(0, x - (K - m));
-          return (int)(num / K);
-        };
-        a = gs + start(j);
-        b = gs + start(j + 1);
-      } else {
-        cta_range(p, tstart, v, a, b);
-      }
+      int a, b;
+      const int v = blockIdx.x;
+      cta_range(p, tstart, v, a, b);
       wsum[0] = a;
       wsum[1] = b;
       wsum[M_VCTA - M_WSUM] = v;
