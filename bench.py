@@ -69,13 +69,13 @@ def parse():
 # (sha256 over the code, comments stripped, of the C header and the decode kernels'
 # translation unit); any other code gives traffic null.
 MEASURED_TRAFFIC = {
-    "long128k": {"bytes": 279792896, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
-    "long128k_scalar": {"bytes": 271406592, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
-    "dense8k": {"bytes": 70021120, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
-    "bf16ctl": {"bytes": 137195776, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
-    "ragged": {"bytes": 144063488, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
-    "sparse": {"bytes": 70827008, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
-    "prefill": {"bytes": 11290624, "csrc_sha256": "4b794f7bc739e1b6d756c4e3fc96444bd2ec06ecba4e1079fb9f38a9425d9946"},
+    "long128k": {"bytes": 279576064, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
+    "long128k_scalar": {"bytes": 271514880, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
+    "dense8k": {"bytes": 69886464, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
+    "bf16ctl": {"bytes": 136982528, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
+    "ragged": {"bytes": 143708672, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
+    "sparse": {"bytes": 70820352, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
+    "prefill": {"bytes": 11239168, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
 }
 
 
