@@ -118,7 +118,9 @@ __device__ __forceinline__ void reset_state(Frag &f) {
 constexpr int kPeMin = -60, kPeMax = 60;
 constexpr int kScalarPe = 8;  // the fixed power of two of P in scalar-scale mode
 
-// online_row with p' = 2^(s - m + pe) = p * 2^pe in s on return; l still sums p.
+// The online softmax step of one row with p' = 2^(s - m + pe) = p * 2^pe in s on return
+// (l still sums p); returns the factor the row's accumulators must be rescaled by (1 when
+// the maximum did not grow).
 template <int N>
 __device__ __forceinline__ float online_row_pe(float (&s)[N], float &m, float &l, int pe) {
   float mx = s[0];
@@ -252,35 +254,11 @@ __device__ __forceinline__ void unfold_rows(Frag &f) {
 
 // ------------------------------------------------------------------------ online softmax
 
-// s holds the log2-domain scores of this lane's columns of one row (tokens 8j + 2t + e
-// of the chunk's n-tiles j, column 2j + e); on return it holds p = 2^(s - m) with m the
-// row's running maximum, and l is updated.  Returns the factor by which the row's
-// accumulators must be rescaled (1 when the maximum did not grow).
-template <int N>
-__device__ __forceinline__ float online_row(float (&s)[N], float &m, float &l) {
-  float mx = s[0];
-#pragma unroll
-  for (int k = 1; k < N; ++k) mx = fmaxf(mx, s[k]);
-  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
-  float alpha = 1.f;
-  if (mx > m) {
-    alpha = fast_exp2(m - mx);
-    m = mx;
-    l *= alpha;
-  }
-  const float ref = (m == -INFINITY) ? 0.f : m;
-#pragma unroll
-  for (int k = 0; k < N; ++k) s[k] = fast_exp2(s[k] - ref);
-  float sum = 0.f;
-#pragma unroll
-  for (int k = 0; k < N; k += 4) sum += (s[k] + s[k + 1]) + (s[k + 2] + s[k + 3]);
-  l += sum;
-  return alpha;
-}
-
-// online_row, then the rescale of the row's accumulators (o[.][half], o[.][half + 1]) in
-// the same branch, for paths whose P needs no further fold.
+// The online softmax step of one row.  s holds the log2-domain scores of this lane's
+// columns of the row (tokens 8j + 2t + e of the chunk's n-tiles j, column 2j + e); on
+// return it holds p = 2^(s - m) with m the row's running maximum, l is updated, and the
+// row's accumulators (o[.][half], o[.][half + 1]) are rescaled in the same branch when the
+// maximum grew.  For paths whose P needs no further fold.
 template <int N>
 __device__ __forceinline__ void online_row_rescale(float (&s)[N], float &m, float &l,
                                                    float (&o)[16][4], int half) {
