@@ -5,9 +5,9 @@
 // warp per page; the request's index query rows against the page's tokens on the tensor
 // cores, mma.sync m16n8k16 in f16 with fp32 accumulation) and writes each (row, page)
 // score: the base-2 log-sum-exp of the page's attended (head, token) scores.  index_select_kernel, a CTA
-// per row, sorts that row's candidate pages by score in shared memory (bitonic, keys of
-// score and page index) with the row's last attended page forced first, and writes the
-// first topk.  HBM-bound on the index cache: 128 B per position per request.
+// per row, sorts that row's candidate pages by score (bitonic, keys of score and page
+// index; the stages within a warp on shuffles, the wider ones in shared memory) with the
+// row's last attended page forced first, and writes the first topk.  HBM-bound on the index cache: 128 B per position per request.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -290,18 +290,61 @@ __global__ void __launch_bounds__(1024) index_select_kernel(const IdxParams p, i
     keys[b] = k;
   }
   __syncthreads();
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int q = tid; q < (n >> 1); q += nt) {
-        const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1)), x = i + j;  // i has bit j clear
-        const unsigned long long a = keys[i], c = keys[x];
-        const bool desc = (i & k) == 0;
-        if (desc ? a < c : a > c) {
-          keys[i] = c;
-          keys[x] = a;
+  if (n == 2 * nt) {
+    // Two keys per thread, elements 2 tid and 2 tid + 1, held in registers: the stages
+    // whose pairs lie within a warp (distance j <= 32) run on shuffles with no barrier,
+    // and only the wider ones (j >= 64) go through shared memory.
+    unsigned long long x0 = keys[2 * tid], x1 = keys[2 * tid + 1];
+    for (int k = 2; k <= n; k <<= 1) {
+      int j = k >> 1;
+      if (j >= 64) {
+        keys[2 * tid] = x0;
+        keys[2 * tid + 1] = x1;
+        __syncthreads();
+        for (; j >= 64; j >>= 1) {  // one pair per thread
+          const int i = ((tid & ~(j - 1)) << 1) | (tid & (j - 1)), x = i + j;
+          const unsigned long long a = keys[i], c = keys[x];
+          const bool desc = (i & k) == 0;
+          if (desc ? a < c : a > c) {
+            keys[i] = c;
+            keys[x] = a;
+          }
+          __syncthreads();
         }
+        x0 = keys[2 * tid];
+        x1 = keys[2 * tid + 1];
       }
-      __syncthreads();
+      // elements e and e ^ j sit in lanes tid and tid ^ (j / 2); the pair's lower element
+      // keeps the larger key in a descending block ((e & k) == 0), the smaller otherwise
+      const bool desc = ((2 * tid) & k) == 0;
+      for (; j >= 2; j >>= 1) {
+        const unsigned long long y0 = __shfl_xor_sync(~0u, x0, j >> 1);
+        const unsigned long long y1 = __shfl_xor_sync(~0u, x1, j >> 1);
+        const bool takemax = (((2 * tid) & j) == 0) == desc;
+        x0 = takemax ? (x0 > y0 ? x0 : y0) : (x0 < y0 ? x0 : y0);
+        x1 = takemax ? (x1 > y1 ? x1 : y1) : (x1 < y1 ? x1 : y1);
+      }
+      const unsigned long long hi = x0 > x1 ? x0 : x1, lo = x0 > x1 ? x1 : x0;  // j = 1
+      x0 = desc ? hi : lo;
+      x1 = desc ? lo : hi;
+    }
+    keys[2 * tid] = x0;
+    keys[2 * tid + 1] = x1;
+    __syncthreads();
+  } else {
+    for (int k = 2; k <= n; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int q = tid; q < (n >> 1); q += nt) {
+          const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1)), x = i + j;  // i has bit j clear
+          const unsigned long long a = keys[i], c = keys[x];
+          const bool desc = (i & k) == 0;
+          if (desc ? a < c : a > c) {
+            keys[i] = c;
+            keys[x] = a;
+          }
+        }
+        __syncthreads();
+      }
     }
   }
   const int cnt = min(nb, p.topk);
