@@ -104,17 +104,19 @@ __device__ __forceinline__ void reset_state(Frag &f) {
 }
 
 // Per-token V scales fold into P per row: P'[j] = p[j] * v_scale[j] * 2^pe, with one power
-// of two per row (and lane quad), kept while the chunk's largest p * v_scale * 2^pe stays
-// within [2^-6, 2^12).  So P' never overflows the f16 operand, and the largest terms of
-// every chunk keep f16's 11 bits, however far apart the tokens' magnitudes (per-token
-// scales of 2^-20 .. 2^20 in one sequence included): the reference is the largest product,
-// not the largest scale, so a token with p = 1 and a small scale is not flushed by a
-// neighbour with a large scale and p ~ 0.  The row's o is accumulated in the same units,
-// and the power of two rides in the exponent of p.  pe is chosen from the chunk's V-scale
-// exponent range and the row's largest p' (online_row_fit), known before the exponentials,
-// without a branch between the softmax and PV; only a chunk whose scales spread wider than
-// 2^15 (or that holds masked tokens) takes an exact test of its P' (refold_row).  pe stays
-// within [-60, 60], which covers V scales of 2^-60 .. 2^64.
+// of two per row (and lane quad), so that P' never overflows the f16 operand however far
+// apart the tokens' magnitudes are (per-token scales of 2^-20 .. 2^20 in one sequence
+// included).  The row's o is accumulated in the same units, and the power of two rides in
+// the exponent of p.  A chunk keeps the rows' powers of two while every weight * 2^pe lies
+// in [2^-3, 2^12): no product reaches 2^12, and the row's p = 1 token, wherever it is,
+// contributes at least 2^-3, so what f16's subnormals can lose on the smallest products
+// stays below 2^-22 of the row's sum per token.  Otherwise pe is placed anew: from the
+// chunk's V-scale exponent range and the row's largest p' (online_row_fit), known before
+// the exponentials, so that the largest products keep f16's 11 bits; a chunk whose scales
+// spread wider than 2^15 (or that holds masked tokens) takes an exact placement on its P'
+// (refold_row).  The reference is the largest product, not the largest scale, so a token
+// with p = 1 and a small scale is not flushed by a neighbour with a large scale and p ~ 0.
+// pe stays within [-60, 60], which covers V scales of 2^-60 .. 2^64.
 constexpr int kPeMin = -60, kPeMax = 60;
 constexpr int kScalarPe = 8;  // the fixed power of two of P in scalar-scale mode
 
@@ -420,19 +422,20 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
   uint32_t pa[NKS][4];
   float a0, a1;
   if (SM == PA_SCALE_PER_TOKEN) {
-    int el, eh;
-    weight_exponents<NC>(vw, el, eh);  // ready long before the softmax needs it
-    if (eh - el <= 15) {  // the same for the whole warp
-      a0 = online_row_fit<NC>(s0, f.m[0], f.l[0], f.pe[0], eh, el);
-      a1 = online_row_fit<NC>(s1, f.m[1], f.l[1], f.pe[1], eh, el);
+    // The rows' powers of two stand while every weight of the chunk keeps its products
+    // below 2^12 and its p = 1 product at or above 2^-3 (a min / max over the lane's
+    // weights and one vote): no search, nothing between the softmax and PV.
+    float vmx = vw[0], vmn = vw[0];
 #pragma unroll
-      for (int k = 0; k < NC; ++k) {
-        s0[k] *= vw[k];
-        s1[k] *= vw[k];
-      }
-    } else {
-      // scales spread wider (or masked tokens, whose weight is 0): each row's window is
-      // settled on its fp32 P'
+    for (int k = 1; k < NC; ++k) {
+      vmx = fmaxf(vmx, vw[k]);
+      vmn = fminf(vmn, vw[k]);
+    }
+    const float u0 = __uint_as_float((uint32_t)(f.pe[0] + 127) << 23);
+    const float u1 = __uint_as_float((uint32_t)(f.pe[1] + 127) << 23);
+    const bool stands = !masked && vmx * u0 < 4096.f && vmx * u1 < 4096.f && vmn * u0 >= 0.125f &&
+                        vmn * u1 >= 0.125f;
+    if (__all_sync(~0u, stands)) {
       a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], f.pe[0]);
       a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], f.pe[1]);
 #pragma unroll
@@ -440,8 +443,30 @@ __device__ __forceinline__ void chunk_fp8(const KParams &p, uint32_t st, int tb,
         s0[k] *= vw[k];
         s1[k] *= vw[k];
       }
-      a0 *= refold_row<NC>(s0, f.pe[0]);
-      a1 *= refold_row<NC>(s1, f.pe[1]);
+    } else {
+      int el, eh;
+      weight_exponents<NC>(vw, el, eh);
+      if (eh - el <= 15) {  // the same for the whole warp
+        a0 = online_row_fit<NC>(s0, f.m[0], f.l[0], f.pe[0], eh, el);
+        a1 = online_row_fit<NC>(s1, f.m[1], f.l[1], f.pe[1], eh, el);
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+          s0[k] *= vw[k];
+          s1[k] *= vw[k];
+        }
+      } else {
+        // scales spread wider (or masked tokens, whose weight is 0): each row's window is
+        // settled on its fp32 P'
+        a0 = online_row_pe<NC>(s0, f.m[0], f.l[0], f.pe[0]);
+        a1 = online_row_pe<NC>(s1, f.m[1], f.l[1], f.pe[1]);
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+          s0[k] *= vw[k];
+          s1[k] *= vw[k];
+        }
+        a0 *= refold_row<NC>(s0, f.pe[0]);
+        a1 *= refold_row<NC>(s1, f.pe[1]);
+      }
     }
   } else {
     // one scale for the whole cache: P' = p * 2^8 (p <= 1) keeps p down to 2^-22 out of
