@@ -69,13 +69,13 @@ def parse():
 # (sha256 over the code, comments stripped, of the C header and the decode kernels'
 # translation unit); any other code gives traffic null.
 MEASURED_TRAFFIC = {
-    "long128k": {"bytes": 279576064, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
-    "long128k_scalar": {"bytes": 271514880, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
-    "dense8k": {"bytes": 69886464, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
-    "bf16ctl": {"bytes": 136982528, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
-    "ragged": {"bytes": 143708672, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
-    "sparse": {"bytes": 70820352, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
-    "prefill": {"bytes": 11239168, "csrc_sha256": "e2667272bac0d9128d32689c5ef258cdfab8fb3959cb4e5bb44a91f4fd3b4e70"},
+    "long128k": {"bytes": 279868160, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
+    "long128k_scalar": {"bytes": 271396352, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
+    "dense8k": {"bytes": 69891840, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
+    "bf16ctl": {"bytes": 137229568, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
+    "ragged": {"bytes": 143697152, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
+    "sparse": {"bytes": 70576896, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
+    "prefill": {"bytes": 11238400, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
 }
 
 
@@ -106,7 +106,7 @@ def csrc_sha256():
 
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
 # The indexer's two launches of one call (score + select), from the same kind of capture.
-MEASURED_TRAFFIC_INDEXER = {"bytes": 557502464, "src_sha256": "10e4ffc6dc675f80623de23a95ba07fa360db36ae91dea431676200ce5b4bf4c"}
+MEASURED_TRAFFIC_INDEXER = {"bytes": 557419776, "src_sha256": "d1faf0e086883c97d081635977351cfb5d123b5f7d14952e9459b62a91092844"}
 MEASURED_TRAFFIC_KV_WRITE = {"bytes": 171386368, "src_sha256": "c0729fd8a04a448779a9dd040359180d545aa1e7f4dfb1cf5afe0cdbaae6cb6f"}
 
 
