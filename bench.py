@@ -57,6 +57,9 @@ def parse():
                     help="with --profile: this many KV copies instead of the rotation's "
                          "(ncu flushes L2 before each captured launch, so one copy keeps a "
                          "capture's device memory small)")
+    ap.add_argument("--trace", action="store_true",
+                    help="diagnostic: with the traced library, the per-CTA launch trace of "
+                         "back-to-back calls of the decode workload (no timing line)")
     ap.add_argument("--only", action="store_true",
                     help="time the selected workload only (no 'workloads' key)")
     ap.add_argument("--extra-steps", type=int, default=200,
@@ -538,6 +541,62 @@ def _extra_workloads(args, dev, stream, local, skip):
     return res
 
 
+TRACE_MARKS = ["entry", "prologue", "producer_wait", "consumer_wait", "first_tile",
+                "last_tile", "partial_stored", "arrived", "merge_start", "merge_end", "exit"]
+
+
+def trace_decode(args, dev, calls=16):
+    """Launch trace of `calls` back-to-back decode calls (one CUDA graph, replayed after a
+    warm replay) with the traced library: for each mark, the median over calls of the
+    median and of the latest CTA, in us after the previous call's last CTA exited."""
+    import ctypes
+    import torch
+    from paged_fp8_kv_04_gb300 import binding, build as libbuild
+    binding._lib = binding.lib(libbuild.build(trace=True))
+    w = _decode_setup(args.workload, dev, tcgen05=False, partition=args.partition)
+    plan, args_list, npools = w["plan"], w["args_list"], w["npools"]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            plan.decode_args(args_list[i % npools], stream=stream)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(calls):
+            plan.decode_args(args_list[i % npools], stream=stream)
+    for _ in range(2):
+        pre_queue(stream)
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize(dev)
+    assert plan.device_status() == 0
+    buf = np.zeros((16, 1024, 16), dtype=np.uint64)
+    st = binding.lib().pa_debug_trace(ctypes.c_void_p(buf.ctypes.data), buf.nbytes)
+    if st != 0:
+        raise RuntimeError(f"pa_debug_trace: status {st}")
+    grid = plan.info()["grid_ctas"]
+    t = buf[:, :grid, :].astype(np.int64)
+    t = t[np.argsort(t[:, 0, 11])]                 # slots in launch order
+    busy = t[-1, :, 13] > t[-1, :, 12]
+    ends = t[:, :, 10].max(axis=1)
+    stats = {m: ([], []) for m in TRACE_MARKS}
+    for c in range(1, t.shape[0]):                 # calls that follow another back to back
+        rel = (t[c] - ends[c - 1]) / 1e3
+        for k, m in enumerate(TRACE_MARKS):
+            v = rel[busy, k]
+            v = v[t[c, busy, k] >= t[c, busy, 0]]     # marks this call reached
+            if v.size:
+                stats[m][0].append(float(np.median(v)))
+                stats[m][1].append(float(np.max(v)))
+    line = {"trace": args.workload, "grid_ctas": int(grid), "busy_ctas": int(busy.sum()),
+            "calls": int(t.shape[0] - 1),
+            "us_per_call": round(float(np.median(np.diff(ends[1:]))) / 1e3, 2),
+            "after_previous_call_us": {m: [round(float(np.median(a)), 2), round(float(np.median(b)), 2)]
+                                       for m, (a, b) in stats.items() if a},
+            "cols": "median CTA, latest CTA (medians over calls)"}
+    print(json.dumps(line), flush=True)
+
+
 def bench_ours(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -560,6 +619,8 @@ def bench_ours(args):
         return bench_kv_write(args, dev, rank, world, local)
     if args.workload == "indexer":
         return bench_indexer(args, dev, rank, world, local)
+    if args.trace:
+        return trace_decode(args, dev)
     w = _decode_setup(args.workload, dev, tcgen05=args.tcgen05, partition=args.partition,
                       pools=args.pools if args.profile else 0)
     p, desc, plan, d, out, keep = w["p"], w["desc"], w["plan"], w["d"], w["out"], w["keep"]

@@ -376,6 +376,18 @@ size_t pa_debug_gather_tile_bytes(const pa_plan_t *plan);
 pa_status_t pa_debug_gather(pa_plan_t *plan, const pa_decode_args_t *args, void *dump,
                             size_t dump_bytes, void *stream);
 
+/* Launch trace of the mma.sync decode kernel, a diagnostic: the GPU global timer (ns) at
+ * fixed points of each CTA's run, kept for each CTA's last 16 launches on the current
+ * device.  Copies min(bytes, 2 MiB) of the array uint64 [16 slots][1024 CTAs][16 marks]
+ * to host memory; slot = the CTA's launch count mod 16.  Marks: 0 entry, 1 prologue (the
+ * schedule) done, 2 producer past the dependency wait, 3 consumers past it, 4 first tile
+ * in warp 0, 5 warp 0 through the CTA's range, 6 partial stored, 7 arrival counted,
+ * 8 / 9 merge start / end, 10 exit, 11 the CTA's launch count, 12 / 13 its tile range
+ * [a, b), 14 merge duty bits; marks a launch does not reach keep older values.  Returns
+ * PA_ERR_UNSUPPORTED unless the library was built with tracing (its kernels carry no
+ * trace code otherwise), PA_ERR_CUDA if the copy fails. */
+pa_status_t pa_debug_trace(void *host, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

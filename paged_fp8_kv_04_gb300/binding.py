@@ -152,6 +152,8 @@ def lib(path: Optional[str] = None):
     L.pa_index_topk.restype = ctypes.c_int
     L.pa_lse_merge.argtypes = [ctypes.POINTER(LseMergeArgs), P]
     L.pa_lse_merge.restype = ctypes.c_int
+    L.pa_debug_trace.argtypes = [P, ctypes.c_size_t]
+    L.pa_debug_trace.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L

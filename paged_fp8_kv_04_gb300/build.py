@@ -12,6 +12,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libpagedfp8.so")
+# The same library with the decode kernel's launch trace compiled in (pa_debug_trace).
+TRACE_LIB_PATH = os.path.join(BUILD_DIR, "libpagedfp8_trace.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -31,21 +33,23 @@ def _inputs():
         [os.path.join(INCLUDE, "pa.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every .cu under csrc/ into one shared library (static cudart)."""
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Compile every .cu under csrc/ into one shared library (static cudart); with trace,
+    the diagnostic variant whose decode kernel records its launch trace."""
+    out = TRACE_LIB_PATH if trace else LIB_PATH
+    if not force and up_to_date(out):
+        return out
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I" + INCLUDE, "-I" + CSRC, "-o", tmp] + sources()
+           "-I" + INCLUDE, "-I" + CSRC, "-o", tmp] + (["-DPA_TRACE"] if trace else []) + sources()
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -53,5 +57,5 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
     if verbose:
         print(res.stdout + res.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out

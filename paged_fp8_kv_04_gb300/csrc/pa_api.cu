@@ -707,3 +707,15 @@ extern "C" pa_status_t pa_decode_noalloc(const pa_plan_desc_t *desc, const pa_de
   if (launch<false>(plan.desc, k, g.smem, s) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
+
+extern "C" pa_status_t pa_debug_trace(void *host, size_t bytes) {
+#ifdef PA_TRACE
+  if (host == nullptr) return PA_ERR_INVALID_ARG;
+  const size_t n = bytes < sizeof(pa::g_trace) ? bytes : sizeof(pa::g_trace);
+  return cudaMemcpyFromSymbol(host, pa::g_trace, n) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+#else
+  (void)host;
+  (void)bytes;
+  return PA_ERR_UNSUPPORTED;
+#endif
+}

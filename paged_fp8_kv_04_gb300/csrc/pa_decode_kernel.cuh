@@ -133,6 +133,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
         if (lane == 0) raise_flag(p, sm, PA_DEV_TIMEOUT);
         break;
       }
+      if (i == 0 && ctid == 0) trace(T_FIRST_TILE);
       have = true;
       const int qs = seg & 1;
       ++seg;
@@ -228,6 +229,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     }
 
     if (!end) continue;
+    if (i == n - 1 && ctid == 0) trace(T_LAST_TILE);  // warp 0 is through the range
 
     // ---- end of this CTA's part of sequence (r, h): merge the token slices -----------
     // The merge generation of a split sequence, read by the threads that may count this
@@ -274,6 +276,7 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
       // A split sequence: store this CTA's partial.
       if (writer) write_partial(p, f, slot, mtile, g, t, lane);
     }
+    if (i == n - 1 && ctid == 0) trace(T_STORED);
     // The partial is stored.  If the sequence ends before the CTA's last tile it is the one
     // the CTA started in the middle of: it is counted at once (the other warps stream on).
     // The sequence the CTA leaves unfinished is counted after the last tile.
@@ -317,6 +320,10 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
     }
   }
   cons_sync(p, sm, cphase);
+  if (ctid == 0) {
+    trace(T_ARRIVED);
+    trace_value(T_LAST, sm.misc()[M_LAST] | (sm.misc()[M_LAST + 1] << 1));
+  }
 #pragma unroll 1
   for (int k = 0; k < 2; ++k) {
     const bool mine_k = k == 0 ? has_head : has_tail;
@@ -333,12 +340,16 @@ __device__ void run_consumer(const KParams &p, const Smem &sm, int a, int b, int
         }
         cons_sync(p, sm, cphase);
       }
+      if (ctid == 0) trace(T_MERGE);
       merge_share<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], sm.misc()[M_VCTA] - rec[4], ctid);
+      if (ctid == 0) trace(T_MERGED);
     } else if (sm.misc()[M_LAST + k]) {
       // a small merge, or CTAs of one sequence in different waves: the last to arrive merges
       // alone (the others exit, and the next launch's CTAs take their SMs meanwhile)
       __threadfence();
+      if (ctid == 0) trace(T_MERGE);
       merge_partials<KVT>(p, hh, rec[2], rec[3], rec[4], rec[5], ctid);
+      if (ctid == 0) trace(T_MERGED);
     }
   }
 }
@@ -364,8 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     for (int k = 0; k < 4; ++k) sm.misc()[M_ZERO + k] = 0;
     fence_barrier_init();
   }
+  if (threadIdx.x == 0) trace(T_ENTRY);
   pdl_launch_dependents();
   const uint32_t fl = scan_tiles(p, sm.tstart(), sm.misc() + M_WSUM);
+  if (threadIdx.x == 0) {
+    trace(T_PROLOGUE);
+    trace_value(T_A, (unsigned)sm.misc()[M_WSUM]);
+    trace_value(T_B, (unsigned)sm.misc()[M_WSUM + 1]);
+  }
   const uint32_t report = blockIdx.x == 0 ? fl : 0u;
   if (warp >= kNCW) {
     regs_dec<kProdRegs>();
@@ -382,8 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   regs_inc<kConsRegs>();
   const int a = sm.misc()[M_WSUM], b = sm.misc()[M_WSUM + 1];
   pdl_wait();  // consumers write outputs and the workspace
+  if (threadIdx.x == 0) trace(T_CONSUMER);
   if (report) atomicOr(p.status, report);
   run_consumer<KVT, SM, DUMP>(p, sm, a, b, warp, lane);
+  if (threadIdx.x == 0) trace_close();
 }
 
 // (request, query token, cutoff) of every row, through request_info -- the same map

@@ -30,6 +30,45 @@
 
 namespace pa {
 
+// Launch trace (compiled in only with PA_TRACE): the global timer at fixed points of each
+// CTA's run, kept for the last kTraceCalls launches of every CTA (slot = the CTA's launch
+// count modulo kTraceCalls).  pa_debug_trace copies it out.  Without PA_TRACE the marks
+// are empty functions.
+enum : int {
+  T_ENTRY = 0, T_PROLOGUE = 1, T_PRODUCER = 2, T_CONSUMER = 3, T_FIRST_TILE = 4,
+  T_LAST_TILE = 5, T_STORED = 6, T_ARRIVED = 7, T_MERGE = 8, T_MERGED = 9, T_EXIT = 10,
+  T_CALL = 11, T_A = 12, T_B = 13, T_LAST = 14, T_MARKS = 16
+};
+constexpr int kTraceCalls = 16, kTraceCtas = 1024;
+#ifdef PA_TRACE
+__device__ unsigned long long g_trace[kTraceCalls][kTraceCtas][T_MARKS];
+__device__ unsigned int g_trace_count[kTraceCtas];
+__device__ __forceinline__ void trace_value(int k, unsigned long long v) {
+  if (blockIdx.x < kTraceCtas) g_trace[g_trace_count[blockIdx.x] % kTraceCalls][blockIdx.x][k] = v;
+}
+__device__ __forceinline__ void trace(int k) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  trace_value(k, t);
+}
+// Ends this CTA's record of the launch (one thread, last).
+__device__ __forceinline__ void trace_close() {
+  if (blockIdx.x < kTraceCtas) {
+    trace_value(T_CALL, g_trace_count[blockIdx.x]);
+    trace(T_EXIT);
+    ++g_trace_count[blockIdx.x];
+  }
+}
+#else
+__device__ __forceinline__ void trace_value(int, unsigned long long) {}
+__device__ __forceinline__ void trace(int) {}
+__device__ __forceinline__ void trace_close() {}
+#endif
+
+}  // namespace pa
+
+namespace pa {
+
 constexpr int kD = 128;          // head_dim
 constexpr int kG = 16;           // query heads per KV head (rows of one m-tile)
 constexpr int kTile = 128;       // tokens per KV tile

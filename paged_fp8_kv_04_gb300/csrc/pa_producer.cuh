@@ -82,6 +82,7 @@ __device__ void run_producer(const KParams &p, const Smem &sm, int a, int b, uin
         }
       }
       pdl_wait();
+      if (lane == 0) trace(T_PRODUCER);
       waited_deps = true;
       if (report) atomicOr(p.status, report);
     }

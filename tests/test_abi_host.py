@@ -355,3 +355,9 @@ def test_oracle_and_cuda_sources_share_nothing():
     for f in (root / "paged_fp8_kv_04_gb300" / "csrc").iterdir():
         text = f.read_text()
         assert "oracle" not in " ".join(re.findall(r'#include\s+[<"]([^>"]+)[>"]', text)), f.name
+
+
+def test_trace_only_in_the_traced_build(lib):
+    # the default build carries no trace code: pa_debug_trace refuses without a GPU call
+    buf = (ctypes.c_uint64 * 16)()
+    assert lib.pa_debug_trace(ctypes.cast(buf, ctypes.c_void_p), ctypes.sizeof(buf)) == 2  # unsupported
