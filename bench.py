@@ -72,13 +72,13 @@ def parse():
 # (sha256 over the code, comments stripped, of the C header and the decode kernels'
 # translation unit); any other code gives traffic null.
 MEASURED_TRAFFIC = {
-    "long128k": {"bytes": 279868160, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
-    "long128k_scalar": {"bytes": 271396352, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
-    "dense8k": {"bytes": 69891840, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
-    "bf16ctl": {"bytes": 137229568, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
-    "ragged": {"bytes": 143697152, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
-    "sparse": {"bytes": 70576896, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
-    "prefill": {"bytes": 11238400, "csrc_sha256": "f70d326709c0f3d2a85e110c4a375da6a92c38ef97e5d127fb2e867685df02d1"},
+    "long128k": {"bytes": 279795712, "csrc_sha256": "4e6a9e7f65c13427e0a29642480a21a0bac6d1e3447b6ab972697edbde97000e"},
+    "long128k_scalar": {"bytes": 271356672, "csrc_sha256": "4e6a9e7f65c13427e0a29642480a21a0bac6d1e3447b6ab972697edbde97000e"},
+    "dense8k": {"bytes": 69845504, "csrc_sha256": "4e6a9e7f65c13427e0a29642480a21a0bac6d1e3447b6ab972697edbde97000e"},
+    "bf16ctl": {"bytes": 137146112, "csrc_sha256": "4e6a9e7f65c13427e0a29642480a21a0bac6d1e3447b6ab972697edbde97000e"},
+    "ragged": {"bytes": 143980288, "csrc_sha256": "4e6a9e7f65c13427e0a29642480a21a0bac6d1e3447b6ab972697edbde97000e"},
+    "sparse": {"bytes": 70723072, "csrc_sha256": "4e6a9e7f65c13427e0a29642480a21a0bac6d1e3447b6ab972697edbde97000e"},
+    "prefill": {"bytes": 11238912, "csrc_sha256": "4e6a9e7f65c13427e0a29642480a21a0bac6d1e3447b6ab972697edbde97000e"},
 }
 
 
@@ -109,8 +109,8 @@ def csrc_sha256():
 
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
 # The indexer's two launches of one call (score + select), from the same kind of capture.
-MEASURED_TRAFFIC_INDEXER = {"bytes": 557419776, "src_sha256": "d1faf0e086883c97d081635977351cfb5d123b5f7d14952e9459b62a91092844"}
-MEASURED_TRAFFIC_KV_WRITE = {"bytes": 171386368, "src_sha256": "c0729fd8a04a448779a9dd040359180d545aa1e7f4dfb1cf5afe0cdbaae6cb6f"}
+MEASURED_TRAFFIC_INDEXER = {"bytes": 557354496, "src_sha256": "5f0d0ddb6afcf0fe6bd5b3a722b14762b06f424000fc657dd7588b3f3c56887b"}
+MEASURED_TRAFFIC_KV_WRITE = {"bytes": 171521280, "src_sha256": "49a3afa5fd2f1b5d646e1a730f4d43126864abe7033fb499ac2c430b677719ee"}
 
 
 def index_sha256():
