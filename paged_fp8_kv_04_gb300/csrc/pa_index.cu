@@ -157,23 +157,30 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
       cp_async4(sb + kStepRows * kD + 4 * lane, p.ks + (int64_t)ph * p.ps + 8 * j0 + lane);
   };
   float mA = -INFINITY, zA = 0.f, mB = -INFINITY, zB = 0.f;
-  auto fold = [&](float v, int pos, int lim, float &m, float &z) {
-    if (pos >= lim) return;
-    if (v > m) {
-      z = z * exp2f(m - v) + 1.f;
-      m = v;
-    } else {
-      z += exp2f(v - m);
-    }
+  // One step's scores of a row (this lane's 2 kStepTiles columns) into the row's running
+  // (max, sum of 2^(s - max)): one maximum, one rescale and an exp2 per score, no branch;
+  // masked positions enter as -inf.
+  auto fold = [&](const float (&v)[2 * kStepTiles], float &m, float &z) {
+    float mx = m;
+#pragma unroll
+    for (int k = 0; k < 2 * kStepTiles; ++k) mx = fmaxf(mx, v[k]);
+    const float ref = mx == -INFINITY ? 0.f : mx;
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2 * kStepTiles; ++k) sum += pa::fast_exp2(v[k] - ref);
+    z = z * pa::fast_exp2(m - ref) + sum;
+    m = mx;
   };
   auto compute = [&](int it, int slot) {
     const int i = it / ngr, j0 = kStepTiles * (it - i * ngr);
     const int pos0 = (bfirst + kWarps * i) * p.ps;
     const uint32_t sb = wring + slot * kStepBytes;
+    float vA[2 * kStepTiles], vB[2 * kStepTiles];
 #pragma unroll
     for (int u = 0; u < kStepTiles; ++u) {
       const int j = j0 + u;
-      if (j >= ntiles) break;
+      vA[2 * u] = vA[2 * u + 1] = vB[2 * u] = vB[2 * u + 1] = -INFINITY;
+      if (j >= ntiles) continue;
       const uint32_t rb = sb + (8 * u + g) * kD;
       const uint4 x0 = pa::lds128(rb + (((2 * t) ^ g) << 4));
       const uint4 x1 = pa::lds128(rb + (((2 * t + 1) ^ g) << 4));
@@ -185,18 +192,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
         pa::e4m3x4_to_f16x2x2(w[kk], b0, b1);
         pa::mma_f16(acc, af[kk], b0, b1);
       }
-      const int tk = 8 * j + 2 * t;
+      const int tk = pos0 + 8 * j + 2 * t;
       float s0 = p.cscale, s1 = p.cscale;
       if (p.ks != nullptr) {
         const float2 kv = pa::lds64f(sb + kStepRows * kD + 4 * (8 * u + 2 * t));
         s0 *= kv.x;
         s1 *= kv.y;
       }
-      fold(acc[0] * s0, pos0 + tk, limA, mA, zA);
-      fold(acc[1] * s1, pos0 + tk + 1, limA, mA, zA);
-      fold(acc[2] * s0, pos0 + tk, limB, mB, zB);
-      fold(acc[3] * s1, pos0 + tk + 1, limB, mB, zB);
+      vA[2 * u] = tk < limA ? acc[0] * s0 : -INFINITY;
+      vA[2 * u + 1] = tk + 1 < limA ? acc[1] * s1 : -INFINITY;
+      vB[2 * u] = tk < limB ? acc[2] * s0 : -INFINITY;
+      vB[2 * u + 1] = tk + 1 < limB ? acc[3] * s1 : -INFINITY;
     }
+    fold(vA, mA, zA);
+    fold(vB, mB, zB);
   };
   auto finish = [&](int i) {  // page i of the warp: combine, write, reset
     const int bpage = bfirst + kWarps * i;
