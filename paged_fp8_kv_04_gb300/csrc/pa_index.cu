@@ -215,8 +215,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
       const float m2A = __shfl_xor_sync(0xffffffffu, mA, o), z2A = __shfl_xor_sync(0xffffffffu, zA, o);
       const float m2B = __shfl_xor_sync(0xffffffffu, mB, o), z2B = __shfl_xor_sync(0xffffffffu, zB, o);
       const float nA = fmaxf(mA, m2A), nB = fmaxf(mB, m2B);
-      zA = (nA == -INFINITY) ? 0.f : zA * exp2f(mA - nA) + z2A * exp2f(m2A - nA);
-      zB = (nB == -INFINITY) ? 0.f : zB * exp2f(mB - nB) + z2B * exp2f(m2B - nB);
+      zA = (nA == -INFINITY) ? 0.f : zA * pa::fast_exp2(mA - nA) + z2A * pa::fast_exp2(m2A - nA);
+      zB = (nB == -INFINITY) ? 0.f : zB * pa::fast_exp2(mB - nB) + z2B * pa::fast_exp2(m2B - nB);
       mA = nA;
       mB = nB;
     }
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) index_score_kernel(const IdxPa
       if (M != -INFINITY)
         for (int h = 0; h < p.H; ++h) {
           const float mh = rowstat[warp][lane * p.H + h][0];
-          if (mh != -INFINITY) Z += rowstat[warp][lane * p.H + h][1] * exp2f(mh - M);
+          if (mh != -INFINITY) Z += rowstat[warp][lane * p.H + h][1] * pa::fast_exp2(mh - M);
         }
       p.scores[(int64_t)(row0 + lane) * p.stride + bpage] =
           (bad || M == -INFINITY) ? -INFINITY : M + log2f(Z);
