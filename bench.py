@@ -109,7 +109,7 @@ def csrc_sha256():
 
 # The same for the quantise-and-write kernel (sha256 over the C header and pa_kv_write.cu).
 # The indexer's two launches of one call (score + select), from the same kind of capture.
-MEASURED_TRAFFIC_INDEXER = {"bytes": 557435904, "src_sha256": "1541d59acd6bc4d92e7293b0b1644eeb0e6caf12c6dd41d32d0d3c3cdf1b189f"}
+MEASURED_TRAFFIC_INDEXER = {"bytes": 557434624, "src_sha256": "a918cb0e5c67066640d7d2684ba2a3b67dcbca4bb89e22515f76e3b672048126"}
 MEASURED_TRAFFIC_KV_WRITE = {"bytes": 171521280, "src_sha256": "49a3afa5fd2f1b5d646e1a730f4d43126864abe7033fb499ac2c430b677719ee"}
 
 
